@@ -1,0 +1,355 @@
+#!/usr/bin/env python
+"""Benchmark of batched draft-token verification (sampling mode) on GB300.
+
+One step = one spec_verify_sample call over the B=256, V=128256, K=5, bf16,
+T=0.7 workload (target logits [256,6,128256], draft logits [256,5,128256]):
+the vocabulary sweep over all 2816 rows plus the per-sequence accept scan and
+replacement/bonus draw.  Inputs are generated once (seeded, synthetic), copied
+to HBM, and the timed region covers exactly --steps calls bracketed by a
+barrier and a device synchronisation, timed with CUDA events.  The inputs
+(722 MB) are larger than the L2 cache, so no flush is needed between steps.
+
+Metric: verified draft positions per second (B*K per call), whole job.
+Also reported: the sweep kernel's achieved HBM bandwidth against the measured
+copy peak (roofline), an end-to-end figure with host<->device copies inside
+the timed region, the SM clocks seen during the run, and the double-precision
+CPU oracle timed on a bounded sample on this host.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B, V, K, T = 256, 128256, 5, 0.7
+WORKLOAD = "spec-verify sampling B=256 V=128256 K=5 bf16 T=0.7 (target+draft logits, accept scan, residual/bonus draw)"
+METRIC = "verified draft positions/s"
+UNIT = "positions/s"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sweep_stats_headline.txt")
+
+
+def sweep_bytes(b=B, k=K, v=V, elem=2):
+    """Algorithmic bytes of one sweep launch: every target and draft row once."""
+    return b * (2 * k + 1) * v * elem
+
+
+def metric_bytes(b=B, k=K, v=V, elem=2):
+    """Bytes of one verify call: one pass over all rows + one stopping target row per sequence."""
+    return (b * (k + 1) * v + b * k * v + b * v) * elem
+
+
+def source_sha() -> str:
+    d = os.path.join(ROOT, "speculative_decoding_verification_52_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram read+write bytes per sweep launch from the committed ncu summary,
+    only if it was taken on the current kernel sources."""
+    try:
+        kv = {}
+        with open(PROFILE_SUMMARY) as f:
+            for line in f:
+                if ":" in line:
+                    k_, v_ = line.split(":", 1)
+                    kv[k_.strip()] = v_.strip()
+        if kv.get("source_sha") != source_sha():
+            return None
+        return int(float(kv["dram_bytes_per_launch"]))
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling in the background."""
+
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for r in csv.reader(io.StringIO(f.read())):
+                if len(r) >= 10:
+                    rows.append([c.strip() for c in r])
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[4]) for r in rows if r[4].replace(".", "").isdigit()), default=None)}
+
+
+def oracle_positions_per_s(batch, budget_s: float, min_seqs: int = 4):
+    """The oracle, as it stands, over sequences of `batch` until ~budget_s of CPU work."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    done, t_used = 0, 0.0
+    while done < batch.B and (t_used < budget_s or done < min_seqs):
+        sl = slice(done, min(batch.B, done + 4))
+        t0 = time.perf_counter()
+        oracle.verify_sample(batch.target[sl], batch.dtype, batch.draft[sl], batch.dtype, False,
+                             np.ascontiguousarray(batch.draft_tokens[sl]), np.ascontiguousarray(batch.uniforms[sl]),
+                             batch.T)
+        t_used += time.perf_counter() - t0
+        done = sl.stop
+    return done * batch.K / t_used, done, t_used
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def run_reference(args, ws, rank):
+    """The oracle arm: the double-precision CPU oracle on this host's cores,
+    each step a bounded sample (4 sequences) of the same workload."""
+    if rank != 0:
+        return
+    from speculative_decoding_verification_52_gb300 import inputs as gen
+    import oracle
+    oracle.build()
+    per_step = 4
+    batch = gen.config_headline(seqs=list(range(per_step)))
+    for _ in range(max(0, args.warmup)):
+        oracle_positions_per_s(batch, 0.0, min_seqs=per_step)
+    t = 0.0
+    for _ in range(args.steps):
+        _, done, dt = oracle_positions_per_s(batch, 0.0, min_seqs=per_step)
+        t += dt
+    value = args.steps * per_step * K / t
+    sample = f"{per_step} of the 256 sequences per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "B": B, "V": V, "K": K, "temperature": T},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import numpy as np
+    import torch
+
+    import speculative_decoding_verification_52_gb300 as sv
+    from speculative_decoding_verification_52_gb300 import inputs as gen
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sv.lib()
+
+    # weak scaling: every rank verifies its own batch of 256 sequences
+    seqs = list(range(rank * B, (rank + 1) * B))
+    batch = gen.config_headline(seqs=seqs)
+
+    def bf(x, pin=False):
+        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory() if pin else t
+
+    h_target, h_draft = bf(batch.target, True), bf(batch.draft, True)
+    h_tok = torch.from_numpy(batch.draft_tokens).pin_memory()
+    h_uni = torch.from_numpy(batch.uniforms).pin_memory()
+    target, draft = h_target.to(dev), h_draft.to(dev)
+    tok, uni = h_tok.to(dev), h_uni.to(dev)
+    out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+    wsb = sv.workspace(sv.spec_workspace_bytes(B, K, V), dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        sv.spec_verify_sample(target, draft, tok, uni, T, out_tokens=out, num_accepted=nacc, workspace_buf=wsb,
+                              stream=stream)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    # keep the GPU busy while the sampler starts (untimed)
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize()
+
+    sv.spec_profile_begin(args.steps)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    sweep_ms, finish_ms, ncalls = sv.spec_profile_end()
+    ms = e0.elapsed_time(e1) / args.steps
+
+    # end to end through the public API: pinned host inputs -> HBM -> verify -> host outputs
+    h_out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    h_nacc = torch.empty((B,), dtype=torch.int32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        target.copy_(h_target, non_blocking=True)
+        draft.copy_(h_draft, non_blocking=True)
+        tok.copy_(h_tok, non_blocking=True)
+        uni.copy_(h_uni, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_nacc.copy_(nacc, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = f0.elapsed_time(f1) / e2e_steps
+    clk = clocks.stop()
+
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, e2e_ms, sweep_ms / max(1, ncalls)], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms, sweep_avg_ms = t.tolist()
+    else:
+        sweep_avg_ms = sweep_ms / max(1, ncalls)
+
+    if rank != 0:
+        return
+    peaks, src = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    achieved = sweep_bytes() / (sweep_avg_ms * 1e-3) / 1e9
+    value = ws * B * K / (ms * 1e-3)
+    cpu = None
+    if ws == 1:
+        cpu_rate, done, cpu_t = oracle_positions_per_s(batch, budget_s=args.cpu_budget)
+        cpu = {"value": cpu_rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{done} of the 256 sequences of the same workload, single-threaded double-precision C "
+                         f"oracle, {cpu_t:.1f} s"}
+    h2d = sum(x.numel() * x.element_size() for x in (h_target, h_draft, h_tok, h_uni))
+    d2h = h_out.numel() * 4 + h_nacc.numel() * 4
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "V": V, "K": K, "temperature": T,
+                   "input_bytes": sweep_bytes(), "metric_bytes_per_step": metric_bytes(),
+                   "metric_GBps": metric_bytes() / (ms * 1e-3) / 1e9,
+                   "metric_frac_of_8TBps": metric_bytes() / (ms * 1e-3) / 8e12,
+                   "l2": "inputs (722 MB) larger than L2; no flush", "parallelism": f"replicas over sequences x{ws}"},
+        "roofline": {"bound": "hbm", "kernel": "sweep_tma_kernel<BF16,BF16,stats>", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "peak_source": f"{src} hbm_gbs",
+                     "traffic": profiled_traffic(), "algorithmic_bytes": sweep_bytes(),
+                     "avg_launch_ms": sweep_avg_ms, "finish_avg_ms": finish_ms / max(1, ncalls)},
+        "e2e": {"value": ws * B * K / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,174 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) batched draft-token
+ * verification library for speculative decoding.
+ *
+ * The operation is the Leviathan/Chen verification step:
+ *   - "Speculative decoding and EAGLE" (aiengineeringfromscratch.com, Phase 10
+ *     lesson 25), section "The concept" (K draft tokens, one target pass over
+ *     K+1 positions, accept the longest matching prefix, one bonus token when
+ *     all K are accepted), section "The exactness rule" (accept x_t if
+ *     r < p(x_t)/q(x_t), else draw from (p - q)+ / ||(p - q)+||_1 and stop;
+ *     greedy case: accept iff argmax(p) == x_t, else emit argmax(p)) and
+ *     section "Tree attention verification" (verify a candidate tree in one
+ *     pass, keep the longest accepted branch);
+ *   - "Speculative decoding: draft, verify, repeat" (Phase 07 lesson 16),
+ *     steps 1-3 (accept_or_reject, residual_dist, bonus token);
+ *   - "Speculative Decoding: from idea to SOTA" (mountainai.tech), section 3
+ *     (alpha(x) = min(1, p(x)/q(x)); p'(x) = max(0, p(x) - q(x)) / sum).
+ *
+ * Conventions shared by every entry point:
+ *   - All array pointers are DEVICE pointers, row-major and contiguous, with
+ *     the vocabulary as the innermost dimension.  The caller owns every buffer;
+ *     the library allocates nothing.  Scratch memory ("workspace") is supplied
+ *     by the caller, sized by spec_workspace_bytes / spec_tree_workspace_bytes.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous on that stream and never synchronise; results are valid
+ *     once the stream has reached the call.  A workspace must not be shared by
+ *     calls that may overlap on the GPU.
+ *   - Argument errors are detected on the host, before any launch, and return
+ *     SPEC_ERR_INVALID_ARG / SPEC_ERR_UNSUPPORTED / SPEC_ERR_WORKSPACE; a
+ *     failed launch returns SPEC_ERR_CUDA.  spec_last_error() then describes it.
+ *   - Bad data is reported per sequence, never by trapping: num_accepted[b] =
+ *     -1 and out_tokens[b, :] = -1 when the sequence has a draft token outside
+ *     [0, V) or its verification reads an invalid row (a row with NaN; for
+ *     softmax rows also +inf or no finite entry).  num_accepted[b] = -2 means an
+ *     internal pipeline wait hit its time limit (every wait in the library is
+ *     bounded).
+ *   - Vector path: rows whose byte length V * elem_size is a multiple of 16 (and
+ *     16-byte aligned base pointers) are streamed with bulk async copies; other
+ *     shapes take a scalar path with identical results.
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, bad temperature, ... */
+  SPEC_ERR_UNSUPPORTED = 2, /* shape beyond a documented limit             */
+  SPEC_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed        */
+  SPEC_ERR_WORKSPACE = 4    /* workspace missing or too small               */
+} spec_status_t;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+typedef enum { SPEC_DRAFT_LOGITS = 0, SPEC_DRAFT_PROBS = 1 } spec_draft_kind_t;
+
+/* Limits.  K (draft length) is 0..SPEC_MAX_K; tree node count 1..SPEC_MAX_TREE_NODES. */
+#define SPEC_MAX_K 31
+#define SPEC_MAX_TREE_NODES 1024
+
+/* Scratch bytes needed by spec_verify_sample / spec_verify_greedy /
+ * spec_debug_residual for a batch of B sequences, draft length K, vocabulary
+ * V.  Pure host function; 0 for invalid sizes. */
+size_t spec_workspace_bytes(int B, int K, int V);
+
+/* Scratch bytes needed by spec_verify_tree_greedy for B sequences of N tree
+ * nodes over vocabulary V.  Pure host function; 0 for invalid sizes. */
+size_t spec_tree_workspace_bytes(int B, int N, int V);
+
+/* Sampling-mode verification of one speculative step for B sequences.
+ *
+ *   target_logits [B, K+1, V] (target_dtype): target logits at the K drafted
+ *       positions and the one after them.
+ *   draft [B, K, V]: draft logits (draft_kind = SPEC_DRAFT_LOGITS, any
+ *       spec_dtype_t) or draft probabilities (SPEC_DRAFT_PROBS, SPEC_F32 only,
+ *       used exactly as given).  May be NULL when K == 0.
+ *   draft_tokens [B, K] int32: the drafted tokens x_t.  May be NULL when K == 0.
+ *   uniforms [B, K+1, 2] float32 in [0, 1): uniforms[b,t,0] drives the accept
+ *       test at position t, uniforms[b,t,1] the replacement draw at the stopping
+ *       position (residual at a rejection, bonus at t == K).
+ *   temperature: > 0 and finite; the target and draft logits are both divided
+ *       by it before the softmax.  temperature == 0 selects the greedy rule
+ *       (identical to spec_verify_greedy; draft and uniforms are then unused).
+ *
+ * Per sequence: p_t = softmax(target[b,t]/T), q_t = softmax(draft[b,t]/T) (or
+ * the given probabilities); for t = 0..K-1 accept x_t iff q_t(x_t) == 0 or
+ * uniforms[b,t,0] < p_t(x_t)/q_t(x_t); at the first rejection draw
+ * v = smallest index whose running sum of w = max(0, p_t - q_t) exceeds
+ * uniforms[b,t,1] * sum(w) (sum(w) == 0 falls back to w = p_t) and stop; if
+ * all K are accepted draw the bonus the same way from p_K.
+ *
+ * Outputs: out_tokens [B, K+1] int32 = the accepted drafts, then the drawn
+ * token, then -1 padding; num_accepted [B] int32 = the number of accepted
+ * drafts (0..K), or -1 / -2 as described above.
+ *
+ * Limits: V >= 1; V <= 393216 (SPEC_ERR_UNSUPPORTED beyond). */
+spec_status_t spec_verify_sample(const void *target_logits, spec_dtype_t target_dtype,
+                                 const void *draft, spec_dtype_t draft_dtype,
+                                 spec_draft_kind_t draft_kind, const int32_t *draft_tokens,
+                                 const float *uniforms, float temperature, int B, int K, int V,
+                                 int32_t *out_tokens, int32_t *num_accepted, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/* Greedy verification ("The exactness rule", greedy case): g_t = argmax of
+ * target row t (lowest index on ties, raw logits, no temperature); accept x_t
+ * while g_t == x_t; emit g_t at the first mismatch, or g_K when all K match.
+ * Shapes and outputs as spec_verify_sample. */
+spec_status_t spec_verify_greedy(const void *target_logits, spec_dtype_t target_dtype,
+                                 const int32_t *draft_tokens, int B, int K, int V,
+                                 int32_t *out_tokens, int32_t *num_accepted, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/* Greedy tree verification ("Tree attention verification").
+ *
+ *   target_logits [B, N, V]: one logit row per tree node; node i's row is the
+ *       target's distribution for the token that follows node i.
+ *   parents [N] int32 (device): parents[0] = -1 (the root), 0 <= parents[i] < i.
+ *   node_tokens [B, N] int32: the token each node proposes (node 0 ignored; a
+ *       token outside [0, V) never matches).
+ *   max_depth: the tree's depth (longest root-to-node edge count); outputs have
+ *       max_depth + 1 columns.
+ *
+ * Node 0 is accepted; node i is accepted iff its parent is and node_tokens[b,i]
+ * == argmax of the parent's row.  The deepest accepted node i* (ties to the
+ * smallest index) is kept: out_tokens [B, max_depth+1] = the tokens on the path
+ * root -> i* (root excluded), then argmax of i*'s row, then -1 padding;
+ * num_accepted [B] = depth(i*); out_path [B, max_depth+1] (optional, may be
+ * NULL) = the node ids on that path (root excluded), -1 padded.  A malformed
+ * topology or a depth above max_depth gives -1 for every sequence. */
+spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t target_dtype,
+                                      const int32_t *parents, const int32_t *node_tokens, int B,
+                                      int N, int V, int max_depth, int32_t *out_tokens,
+                                      int32_t *num_accepted, int32_t *out_path, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/* Diagnostic twin of spec_verify_sample: runs the same pipeline, but forces
+ * sequence `debug_b` to stop at position `debug_t` (0..K; K = the bonus row)
+ * and writes the normalised replacement distribution the device computed
+ * there, w / sum(w) as float32, to out_row [V] (device), and sum(w) to
+ * out_mass [1] (device).  out_tokens / num_accepted receive the pipeline's
+ * outputs (sequence debug_b's entry reflects the forced stop). */
+spec_status_t spec_debug_residual(const void *target_logits, spec_dtype_t target_dtype,
+                                  const void *draft, spec_dtype_t draft_dtype,
+                                  spec_draft_kind_t draft_kind, const int32_t *draft_tokens,
+                                  const float *uniforms, float temperature, int B, int K, int V,
+                                  int debug_b, int debug_t, float *out_row, float *out_mass,
+                                  int32_t *out_tokens, int32_t *num_accepted, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/* Timing hooks for benchmarks: while enabled, each verify call records CUDA
+ * events around its vocabulary-sweep kernel and around its finishing kernel on
+ * the call's stream (at most max_calls calls are recorded).  spec_profile_end
+ * synchronises on the recorded events and returns the summed milliseconds of
+ * each part and the number of recorded calls.  Not thread-safe. */
+spec_status_t spec_profile_begin(int max_calls);
+spec_status_t spec_profile_end(float *sweep_ms, float *finish_ms, int *calls);
+
+/* Human-readable name of a status; description of the most recent failure on
+ * the calling thread. */
+const char *spec_status_string(spec_status_t status);
+const char *spec_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,576 @@
+// spec_verify.cu -- host side of the C ABI declared in include/spec_verify.h:
+// argument validation, workspace layout, launch configuration, kernel dispatch.
+//
+// Pipeline of one call (all launches on the caller's stream, no sync):
+//   1. sweep      persistent grid over every (row, slice) unit: per-slice
+//                 softmax-normaliser partials (sampling) or argmax partials
+//                 (greedy, tree) into the workspace;
+//   2. finish     per-sequence decisions: the greedy chain rule (one warp per
+//                 sequence), the greedy tree rule (one CTA per sequence) or the
+//                 sampling rule (one thread-block cluster per sequence, which
+//                 re-reads only the stopping row pair).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "finish.cuh"
+#include "spec_verify.h"
+#include "sweep.cuh"
+
+namespace {
+
+using namespace sv;
+
+thread_local char g_err[512] = "";
+
+spec_status_t fail(spec_status_t s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+spec_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(SPEC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMinSlice = 2048;            // smallest sweep slice (elements)
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitNs = 1000000000ull;   // bounded waits: 1 s
+
+int max_slices(int V) { return std::max(1, (V + kMinSlice - 1) / kMinSlice); }
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+struct DevInfo {
+  bool ready = false;
+  int sms = 0;
+  int max_cluster = 8;
+};
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+
+// per-kernel one-time attribute setup, per device
+template <class F>
+bool once_per_device(int dev, F&& f) {
+  static bool done[kMaxDevices] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 0 || dev >= kMaxDevices) return false;
+  if (!done[dev]) {
+    if (!f()) return false;
+    done[dev] = true;
+  }
+  return true;
+}
+
+spec_status_t device_info(DevInfo& out, int& dev) {
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(SPEC_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    int major = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (major < 10) return fail(SPEC_ERR_UNSUPPORTED, "compute capability %d.x: this library is built for sm_103a", major);
+    d.ready = true;
+  }
+  out = d;
+  return SPEC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// sweep configuration
+// ---------------------------------------------------------------------------
+// Pick the slice count S: slices of 8k-32k elements, enough units to cover the
+// grid, and the least tail imbalance (max units per CTA x slice length).
+void choose_slices(int V, long long rows, int grid, int& S, int& L) {
+  const int smax = max_slices(V);
+  int lo = std::max(1, ceil_div(V, 32768));
+  lo = std::max(lo, static_cast<int>(std::min<long long>(smax, (grid + rows - 1) / rows)));
+  lo = std::min(lo, smax);
+  int hi = std::max(lo, std::min(smax, ceil_div(V, 8192)));
+  long long best_cost = -1;
+  S = lo;
+  L = V;
+  for (int s = lo; s <= hi; ++s) {
+    int l = ceil_div(V, s);
+    l = (l + 7) / 8 * 8;
+    const int s_eff = ceil_div(V, l);
+    const long long units = rows * s_eff;
+    const long long per_cta = (units + grid - 1) / grid;
+    const long long cost = per_cta * l;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      S = s_eff;
+      L = l;
+    }
+  }
+}
+
+// occupancy of the TMA sweep (resident CTAs per SM); also sets its shared-memory limit
+template <class TA, class TB, int MODE>
+int sweep_per_sm(int dev) {
+  static int per_sm[kMaxDevices];
+  auto kern = sweep_tma_kernel<TA, TB, MODE>;
+  once_per_device(dev, [&] {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SW_SMEM) != cudaSuccess) return false;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, SW_THREADS, SW_SMEM) != cudaSuccess) return false;
+    per_sm[dev] = std::max(1, n);
+    return true;
+  });
+  return per_sm[dev];
+}
+
+// Launch the sweep over rows [seg0 rows0 | seg1 rows1]; returns the slice count used.
+template <class TA, class TB, int MODE>
+spec_status_t launch_sweep(const DevInfo& di, int dev, bool vec, const unsigned char* seg0, long long rows0,
+                           const unsigned char* seg1, long long rows1, int V, float c, float2* part,
+                           cudaStream_t st, int& S_out) {
+  const long long rows = rows0 + rows1;
+  SweepArgs a{};
+  a.seg0 = seg0;
+  a.seg1 = seg1;
+  a.rows0 = rows0;
+  a.V = V;
+  a.c = c;
+  a.part = part;
+  a.timeout_ns = kWaitNs;
+  if (vec) {
+    const int per_sm = sweep_per_sm<TA, TB, MODE>(dev);
+    if (per_sm <= 0) return fail(SPEC_ERR_CUDA, "sweep kernel setup failed: %s", cudaGetErrorString(cudaGetLastError()));
+    const int grid_cap = di.sms * per_sm;
+    choose_slices(V, rows, grid_cap, a.S, a.L);
+    a.units = rows * a.S;
+    const int grid = static_cast<int>(std::min<long long>(a.units, grid_cap));
+    sweep_tma_kernel<TA, TB, MODE><<<grid, SW_THREADS, SW_SMEM, st>>>(a);
+  } else {
+    const int grid_cap = di.sms * 8;
+    choose_slices(V, rows, grid_cap, a.S, a.L);
+    a.units = rows * a.S;
+    const int grid = static_cast<int>(std::min<long long>(a.units, grid_cap));
+    sweep_scalar_kernel<TA, TB, MODE><<<grid, SS_THREADS, 0, st>>>(a);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "sweep launch");
+  S_out = a.S;
+  return SPEC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// profiling events
+// ---------------------------------------------------------------------------
+struct Prof {
+  bool on = false;
+  int max_calls = 0;
+  int calls = 0;
+  std::vector<cudaEvent_t> ev;
+} g_prof;
+
+void prof_mark(int slot, cudaStream_t st) {
+  if (!g_prof.on || g_prof.calls >= g_prof.max_calls) return;
+  cudaEventRecord(g_prof.ev[3 * g_prof.calls + slot], st);
+  if (slot == 2) ++g_prof.calls;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int esz_of(spec_dtype_t d) { return d == SPEC_BF16 ? 2 : 4; }
+bool dtype_ok(spec_dtype_t d) { return d == SPEC_F32 || d == SPEC_BF16; }
+
+// ---------------------------------------------------------------------------
+// greedy chain
+// ---------------------------------------------------------------------------
+template <class T>
+spec_status_t run_greedy(const DevInfo& di, int dev, const void* target, const int32_t* tokens, int B, int K, int V,
+                         int32_t* out, int32_t* nacc, void* ws, cudaStream_t st) {
+  const bool vec = aligned16(target) && (static_cast<long long>(V) * T::esz) % 16 == 0;
+  const long long rows = static_cast<long long>(B) * (K + 1);
+  float2* part = reinterpret_cast<float2*>(ws);
+  prof_mark(0, st);
+  int S = 0;
+  spec_status_t s = launch_sweep<T, T, MODE_ARGMAX>(di, dev, vec, static_cast<const unsigned char*>(target), rows,
+                                                    nullptr, 0, V, 0.f, part, st, S);
+  if (s != SPEC_OK) return s;
+  prof_mark(1, st);
+  FinishGreedyArgs a{};
+  a.part = part;
+  a.tokens = tokens;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.S = S;
+  a.out_tokens = out;
+  a.num_accepted = nacc;
+  finish_greedy_kernel<<<ceil_div(B, FG_THREADS / 32), FG_THREADS, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "greedy finish launch");
+  prof_mark(2, st);
+  return SPEC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// sampling
+// ---------------------------------------------------------------------------
+template <class TP, class TQ, bool PROBS, bool VEC>
+spec_status_t launch_finish_sample(const DevInfo& di, int dev, const FinishSampleArgs& a, int CL, cudaStream_t st) {
+  auto kern = finish_sample_kernel<TP, TQ, PROBS, VEC>;
+  const size_t smem = fs_smem_bytes(a.L);
+  if (!once_per_device(dev, [&] {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return false;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(fs_smem_bytes(FS_MAX_L))) != cudaSuccess)
+          return false;
+        return true;
+      }))
+    return fail(SPEC_ERR_CUDA, "finish kernel setup failed: %s", cudaGetErrorString(cudaGetLastError()));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B) * CL);
+  cfg.blockDim = dim3(FS_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return cuda_fail(e, "sampling finish launch");
+  return SPEC_OK;
+}
+
+// largest usable cluster size for the sampling finisher on this device
+template <class TP, class TQ, bool PROBS, bool VEC>
+int finish_max_cluster(int dev) {
+  static int mc[kMaxDevices];
+  auto kern = finish_sample_kernel<TP, TQ, PROBS, VEC>;
+  once_per_device(dev, [&] {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(fs_smem_bytes(FS_MAX_L)));
+    mc[dev] = 8;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16);
+    cfg.blockDim = dim3(FS_THREADS);
+    cfg.dynamicSmemBytes = fs_smem_bytes(FS_MAX_L);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) mc[dev] = 16;
+    cudaGetLastError();
+    return true;
+  });
+  return mc[dev] > 0 ? mc[dev] : 8;
+}
+
+template <class TP, class TQ, bool PROBS>
+spec_status_t run_sample(const DevInfo& di, int dev, const void* target, const void* draft, const int32_t* tokens,
+                         const float* uni, float T, int B, int K, int V, int32_t* out, int32_t* nacc, void* ws,
+                         int debug_b, int debug_t, float* debug_row, float* debug_mass, cudaStream_t st) {
+  constexpr int QE = PROBS ? 4 : TQ::esz;
+  const bool vec = aligned16(target) && (static_cast<long long>(V) * TP::esz) % 16 == 0 &&
+                   (K == 0 || (aligned16(draft) && (static_cast<long long>(V) * QE) % 16 == 0));
+  const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+  const long long rows0 = static_cast<long long>(B) * (K + 1);
+  const long long rows1 = PROBS ? 0 : static_cast<long long>(B) * K;
+  float2* part = reinterpret_cast<float2*>(ws);
+  prof_mark(0, st);
+  int S = 0;
+  spec_status_t s = launch_sweep<TP, TQ, MODE_STATS>(di, dev, vec, static_cast<const unsigned char*>(target), rows0,
+                                                     static_cast<const unsigned char*>(draft), rows1, V, c, part, st, S);
+  if (s != SPEC_OK) return s;
+  prof_mark(1, st);
+
+  FinishSampleArgs a{};
+  a.target = static_cast<const unsigned char*>(target);
+  a.draft = static_cast<const unsigned char*>(draft);
+  a.tokens = tokens;
+  a.uni = uni;
+  a.part = part;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.S = S;
+  a.c = c;
+  a.out_tokens = out;
+  a.num_accepted = nacc;
+  a.debug_b = debug_b;
+  a.debug_t = debug_t;
+  a.debug_row = debug_row;
+  a.debug_mass = debug_mass;
+
+  const int maxcl = vec ? finish_max_cluster<TP, TQ, PROBS, true>(dev) : finish_max_cluster<TP, TQ, PROBS, false>(dev);
+  int CL = std::min(maxcl, std::max(1, ceil_div(V, 8192)));
+  int L = (ceil_div(V, CL) + 7) / 8 * 8;
+  while (L > FS_MAX_L && CL < maxcl) {
+    ++CL;
+    L = (ceil_div(V, CL) + 7) / 8 * 8;
+  }
+  if (L > FS_MAX_L) return fail(SPEC_ERR_UNSUPPORTED, "V=%d exceeds the sampling limit (%d)", V, FS_MAX_L * maxcl);
+  a.L = L;
+  s = vec ? launch_finish_sample<TP, TQ, PROBS, true>(di, dev, a, CL, st)
+          : launch_finish_sample<TP, TQ, PROBS, false>(di, dev, a, CL, st);
+  if (s != SPEC_OK) return s;
+  prof_mark(2, st);
+  return SPEC_OK;
+}
+
+spec_status_t dispatch_sample(const DevInfo& di, int dev, const void* target, spec_dtype_t tdt, const void* draft,
+                              spec_dtype_t ddt, spec_draft_kind_t kind, const int32_t* tokens, const float* uni,
+                              float T, int B, int K, int V, int32_t* out, int32_t* nacc, void* ws, int debug_b,
+                              int debug_t, float* drow, float* dmass, cudaStream_t st) {
+#define SV_RUN(TP, TQ, PR) \
+  run_sample<TP, TQ, PR>(di, dev, target, draft, tokens, uni, T, B, K, V, out, nacc, ws, debug_b, debug_t, drow, dmass, st)
+  const bool probs = kind == SPEC_DRAFT_PROBS;
+  if (tdt == SPEC_BF16) {
+    if (probs) return SV_RUN(BF16T, F32T, true);
+    return ddt == SPEC_BF16 ? SV_RUN(BF16T, BF16T, false) : SV_RUN(BF16T, F32T, false);
+  }
+  if (probs) return SV_RUN(F32T, F32T, true);
+  return ddt == SPEC_BF16 ? SV_RUN(F32T, BF16T, false) : SV_RUN(F32T, F32T, false);
+#undef SV_RUN
+}
+
+spec_status_t check_chain_args(const void* target, spec_dtype_t tdt, const int32_t* tokens, int B, int K, int V,
+                               int32_t* out, int32_t* nacc) {
+  if (B < 0) return fail(SPEC_ERR_INVALID_ARG, "B=%d must be >= 0", B);
+  if (K < 0 || K > SPEC_MAX_K) return fail(SPEC_ERR_INVALID_ARG, "K=%d outside [0, %d]", K, SPEC_MAX_K);
+  if (V < 1) return fail(SPEC_ERR_INVALID_ARG, "V=%d must be >= 1", V);
+  if (!dtype_ok(tdt)) return fail(SPEC_ERR_INVALID_ARG, "bad target dtype %d", static_cast<int>(tdt));
+  if (B == 0) return SPEC_OK;
+  if (!target || !out || !nacc) return fail(SPEC_ERR_INVALID_ARG, "NULL target/out_tokens/num_accepted");
+  if (K > 0 && !tokens) return fail(SPEC_ERR_INVALID_ARG, "NULL draft_tokens with K > 0");
+  if (static_cast<long long>(B) * (2 * K + 1) * static_cast<long long>(max_slices(V)) > (1LL << 40))
+    return fail(SPEC_ERR_UNSUPPORTED, "batch too large");
+  return SPEC_OK;
+}
+
+spec_status_t check_ws(void* ws, size_t have, size_t need) {
+  if (need == 0) return SPEC_OK;
+  if (!ws) return fail(SPEC_ERR_WORKSPACE, "NULL workspace (need %zu bytes)", need);
+  if (!aligned16(ws)) return fail(SPEC_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+  if (have < need) return fail(SPEC_ERR_WORKSPACE, "workspace %zu bytes < required %zu", have, need);
+  return SPEC_OK;
+}
+
+spec_status_t sample_entry(const void* target, spec_dtype_t tdt, const void* draft, spec_dtype_t ddt,
+                           spec_draft_kind_t kind, const int32_t* tokens, const float* uni, float T, int B, int K,
+                           int V, int32_t* out, int32_t* nacc, void* ws, size_t wsb, int debug_b, int debug_t,
+                           float* drow, float* dmass, void* stream) {
+  spec_status_t s = check_chain_args(target, tdt, tokens, B, K, V, out, nacc);
+  if (s != SPEC_OK || B == 0) return s;
+  if (!(T >= 0.f) || !std::isfinite(T)) return fail(SPEC_ERR_INVALID_ARG, "temperature %g must be finite and >= 0", T);
+  if (T > 0.f && T < 1e-4f) return fail(SPEC_ERR_UNSUPPORTED, "temperature %g below 1e-4", T);
+  if (kind != SPEC_DRAFT_LOGITS && kind != SPEC_DRAFT_PROBS) return fail(SPEC_ERR_INVALID_ARG, "bad draft kind");
+  if (kind == SPEC_DRAFT_PROBS && ddt != SPEC_F32) return fail(SPEC_ERR_INVALID_ARG, "draft probabilities must be f32");
+  if (K > 0 && !dtype_ok(ddt)) return fail(SPEC_ERR_INVALID_ARG, "bad draft dtype %d", static_cast<int>(ddt));
+  if (T > 0.f && (!uni || (K > 0 && !draft))) return fail(SPEC_ERR_INVALID_ARG, "NULL draft/uniforms");
+  s = check_ws(ws, wsb, spec_workspace_bytes(B, K, V));
+  if (s != SPEC_OK) return s;
+  int dev;
+  DevInfo di;
+  s = device_info(di, dev);
+  if (s != SPEC_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0.f) {
+    return tdt == SPEC_BF16 ? run_greedy<BF16T>(di, dev, target, tokens, B, K, V, out, nacc, ws, st)
+                            : run_greedy<F32T>(di, dev, target, tokens, B, K, V, out, nacc, ws, st);
+  }
+  if (V > FS_MAX_L * 16) return fail(SPEC_ERR_UNSUPPORTED, "V=%d above the sampling limit %d", V, FS_MAX_L * 16);
+  return dispatch_sample(di, dev, target, tdt, draft, K > 0 ? ddt : SPEC_F32, kind, tokens, uni, T, B, K, V, out,
+                         nacc, ws, debug_b, debug_t, drow, dmass, st);
+}
+
+}  // namespace
+
+// ===========================================================================
+// exported C ABI
+// ===========================================================================
+extern "C" {
+
+size_t spec_workspace_bytes(int B, int K, int V) {
+  if (B < 0 || K < 0 || K > SPEC_MAX_K || V < 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(2 * K + 1);
+  return align_up(rows * static_cast<size_t>(max_slices(V)) * sizeof(float2), 256);
+}
+
+size_t spec_tree_workspace_bytes(int B, int N, int V) {
+  if (B < 0 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(N);
+  return align_up(rows * static_cast<size_t>(max_slices(V)) * sizeof(float2), 256);
+}
+
+spec_status_t spec_verify_sample(const void* target_logits, spec_dtype_t target_dtype, const void* draft,
+                                 spec_dtype_t draft_dtype, spec_draft_kind_t draft_kind, const int32_t* draft_tokens,
+                                 const float* uniforms, float temperature, int B, int K, int V, int32_t* out_tokens,
+                                 int32_t* num_accepted, void* workspace, size_t workspace_bytes, void* stream) {
+  try {
+    return sample_entry(target_logits, target_dtype, draft, draft_dtype, draft_kind, draft_tokens, uniforms,
+                        temperature, B, K, V, out_tokens, num_accepted, workspace, workspace_bytes, -1, -1, nullptr,
+                        nullptr, stream);
+  } catch (...) {
+    return fail(SPEC_ERR_CUDA, "unexpected host exception");
+  }
+}
+
+spec_status_t spec_debug_residual(const void* target_logits, spec_dtype_t target_dtype, const void* draft,
+                                  spec_dtype_t draft_dtype, spec_draft_kind_t draft_kind, const int32_t* draft_tokens,
+                                  const float* uniforms, float temperature, int B, int K, int V, int debug_b,
+                                  int debug_t, float* out_row, float* out_mass, int32_t* out_tokens,
+                                  int32_t* num_accepted, void* workspace, size_t workspace_bytes, void* stream) {
+  try {
+    if (debug_b < 0 || debug_b >= B || debug_t < 0 || debug_t > K)
+      return fail(SPEC_ERR_INVALID_ARG, "debug position (%d, %d) outside the batch", debug_b, debug_t);
+    if (!out_row || !out_mass) return fail(SPEC_ERR_INVALID_ARG, "NULL out_row/out_mass");
+    if (!(temperature > 0.f)) return fail(SPEC_ERR_INVALID_ARG, "the residual needs temperature > 0");
+    return sample_entry(target_logits, target_dtype, draft, draft_dtype, draft_kind, draft_tokens, uniforms,
+                        temperature, B, K, V, out_tokens, num_accepted, workspace, workspace_bytes, debug_b, debug_t,
+                        out_row, out_mass, stream);
+  } catch (...) {
+    return fail(SPEC_ERR_CUDA, "unexpected host exception");
+  }
+}
+
+spec_status_t spec_verify_greedy(const void* target_logits, spec_dtype_t target_dtype, const int32_t* draft_tokens,
+                                 int B, int K, int V, int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  try {
+    spec_status_t s = check_chain_args(target_logits, target_dtype, draft_tokens, B, K, V, out_tokens, num_accepted);
+    if (s != SPEC_OK || B == 0) return s;
+    s = check_ws(workspace, workspace_bytes, spec_workspace_bytes(B, K, V));
+    if (s != SPEC_OK) return s;
+    int dev;
+    DevInfo di;
+    s = device_info(di, dev);
+    if (s != SPEC_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return target_dtype == SPEC_BF16
+               ? run_greedy<BF16T>(di, dev, target_logits, draft_tokens, B, K, V, out_tokens, num_accepted, workspace, st)
+               : run_greedy<F32T>(di, dev, target_logits, draft_tokens, B, K, V, out_tokens, num_accepted, workspace, st);
+  } catch (...) {
+    return fail(SPEC_ERR_CUDA, "unexpected host exception");
+  }
+}
+
+spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t target_dtype, const int32_t* parents,
+                                      const int32_t* node_tokens, int B, int N, int V, int max_depth,
+                                      int32_t* out_tokens, int32_t* num_accepted, int32_t* out_path, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  try {
+    if (B < 0) return fail(SPEC_ERR_INVALID_ARG, "B=%d must be >= 0", B);
+    if (N < 1 || N > SPEC_MAX_TREE_NODES) return fail(SPEC_ERR_INVALID_ARG, "N=%d outside [1, %d]", N, SPEC_MAX_TREE_NODES);
+    if (V < 1) return fail(SPEC_ERR_INVALID_ARG, "V=%d must be >= 1", V);
+    if (max_depth < 0 || max_depth >= N) return fail(SPEC_ERR_INVALID_ARG, "max_depth=%d outside [0, N)", max_depth);
+    if (!dtype_ok(target_dtype)) return fail(SPEC_ERR_INVALID_ARG, "bad target dtype");
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || !parents || !node_tokens || !out_tokens || !num_accepted)
+      return fail(SPEC_ERR_INVALID_ARG, "NULL pointer argument");
+    spec_status_t s = check_ws(workspace, workspace_bytes, spec_tree_workspace_bytes(B, N, V));
+    if (s != SPEC_OK) return s;
+    int dev;
+    DevInfo di;
+    s = device_info(di, dev);
+    if (s != SPEC_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long rows = static_cast<long long>(B) * N;
+    const int esz = esz_of(target_dtype);
+    const bool vec = aligned16(target_logits) && (static_cast<long long>(V) * esz) % 16 == 0;
+    float2* part = reinterpret_cast<float2*>(workspace);
+    prof_mark(0, st);
+    int S = 0;
+    if (target_dtype == SPEC_BF16)
+      s = launch_sweep<BF16T, BF16T, MODE_ARGMAX>(di, dev, vec, static_cast<const unsigned char*>(target_logits), rows,
+                                                  nullptr, 0, V, 0.f, part, st, S);
+    else
+      s = launch_sweep<F32T, F32T, MODE_ARGMAX>(di, dev, vec, static_cast<const unsigned char*>(target_logits), rows,
+                                                nullptr, 0, V, 0.f, part, st, S);
+    if (s != SPEC_OK) return s;
+    prof_mark(1, st);
+    FinishTreeArgs a{};
+    a.part = part;
+    a.parents = parents;
+    a.node_tokens = node_tokens;
+    a.B = B;
+    a.N = N;
+    a.V = V;
+    a.S = S;
+    a.max_depth = max_depth;
+    a.out_tokens = out_tokens;
+    a.num_accepted = num_accepted;
+    a.out_path = out_path;
+    finish_tree_kernel<<<B, FT_THREADS, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "tree finish launch");
+    prof_mark(2, st);
+    return SPEC_OK;
+  } catch (...) {
+    return fail(SPEC_ERR_CUDA, "unexpected host exception");
+  }
+}
+
+spec_status_t spec_profile_begin(int max_calls) {
+  if (max_calls < 1) return fail(SPEC_ERR_INVALID_ARG, "max_calls must be >= 1");
+  for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+  g_prof = Prof{};
+  g_prof.ev.resize(static_cast<size_t>(3) * max_calls);
+  for (auto& e : g_prof.ev) {
+    cudaError_t r = cudaEventCreate(&e);
+    if (r != cudaSuccess) return cuda_fail(r, "cudaEventCreate");
+  }
+  g_prof.max_calls = max_calls;
+  g_prof.on = true;
+  return SPEC_OK;
+}
+
+spec_status_t spec_profile_end(float* sweep_ms, float* finish_ms, int* calls) {
+  if (!g_prof.on) return fail(SPEC_ERR_INVALID_ARG, "profiling was not started");
+  g_prof.on = false;
+  double a = 0.0, b = 0.0;
+  for (int i = 0; i < g_prof.calls; ++i) {
+    float t0 = 0.f, t1 = 0.f;
+    cudaError_t r = cudaEventSynchronize(g_prof.ev[3 * i + 2]);
+    if (r != cudaSuccess) return cuda_fail(r, "cudaEventSynchronize");
+    cudaEventElapsedTime(&t0, g_prof.ev[3 * i], g_prof.ev[3 * i + 1]);
+    cudaEventElapsedTime(&t1, g_prof.ev[3 * i + 1], g_prof.ev[3 * i + 2]);
+    a += t0;
+    b += t1;
+  }
+  if (sweep_ms) *sweep_ms = static_cast<float>(a);
+  if (finish_ms) *finish_ms = static_cast<float>(b);
+  if (calls) *calls = g_prof.calls;
+  for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.clear();
+  return SPEC_OK;
+}
+
+const char* spec_status_string(spec_status_t s) {
+  switch (s) {
+    case SPEC_OK: return "SPEC_OK";
+    case SPEC_ERR_INVALID_ARG: return "SPEC_ERR_INVALID_ARG";
+    case SPEC_ERR_UNSUPPORTED: return "SPEC_ERR_UNSUPPORTED";
+    case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA";
+    case SPEC_ERR_WORKSPACE: return "SPEC_ERR_WORKSPACE";
+  }
+  return "SPEC_ERR_UNKNOWN";
+}
+
+const char* spec_last_error(void) { return g_err; }
+
+}  // extern "C"

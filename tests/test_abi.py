@@ -1,0 +1,98 @@
+"""The C-ABI library on the host (no GPU needed): it builds, loads, exports
+every function include/spec_verify.h declares, sizes workspaces, and rejects
+bad arguments before touching the device."""
+import ctypes
+
+import pytest
+
+from speculative_decoding_verification_52_gb300 import binding as B
+from speculative_decoding_verification_52_gb300 import build as build_mod
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_mod.build()
+    return B.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = B.declared_functions()
+    assert {"spec_verify_sample", "spec_verify_greedy", "spec_verify_tree_greedy",
+            "spec_workspace_bytes", "spec_debug_residual"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/spec_verify.h but not exported"
+
+
+def test_workspace_sizes(L):
+    # partial slots: rows x ceil(V / 2048) x 8 bytes, 256-aligned
+    assert L.spec_workspace_bytes(256, 5, 128256) == 2816 * 63 * 8
+    assert L.spec_workspace_bytes(1, 0, 8) == 256
+    assert L.spec_tree_workspace_bytes(128, 64, 128256) == 128 * 64 * 63 * 8
+    for bad in [(-1, 4, 10), (1, -1, 10), (1, 32, 10), (1, 4, 0)]:
+        assert L.spec_workspace_bytes(*bad) == 0
+    assert L.spec_tree_workspace_bytes(1, 0, 10) == 0
+    assert L.spec_tree_workspace_bytes(1, 1025, 10) == 0
+
+
+def _sample(L, **kw):
+    a = dict(target=1 << 20, tdt=1, draft=1 << 21, ddt=1, kind=0, tokens=1 << 22, uni=1 << 23, T=0.7,
+             B=2, K=3, V=64, out=1 << 24, nacc=1 << 25, ws=1 << 26, wsb=1 << 20)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return L.spec_verify_sample(P(a["target"]), a["tdt"], P(a["draft"]), a["ddt"], a["kind"], P(a["tokens"]),
+                                P(a["uni"]), a["T"], a["B"], a["K"], a["V"], P(a["out"]), P(a["nacc"]),
+                                P(a["ws"]), a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=32), B.SPEC_ERR_INVALID_ARG),
+    (dict(K=-1), B.SPEC_ERR_INVALID_ARG),
+    (dict(V=0), B.SPEC_ERR_INVALID_ARG),
+    (dict(B=-3), B.SPEC_ERR_INVALID_ARG),
+    (dict(T=float("nan")), B.SPEC_ERR_INVALID_ARG),
+    (dict(T=-1.0), B.SPEC_ERR_INVALID_ARG),
+    (dict(T=float("inf")), B.SPEC_ERR_INVALID_ARG),
+    (dict(tdt=7), B.SPEC_ERR_INVALID_ARG),
+    (dict(kind=1, ddt=1), B.SPEC_ERR_INVALID_ARG),   # probabilities must be f32
+    (dict(target=0), B.SPEC_ERR_INVALID_ARG),
+    (dict(tokens=0), B.SPEC_ERR_INVALID_ARG),
+    (dict(uni=0), B.SPEC_ERR_INVALID_ARG),
+    (dict(ws=0), B.SPEC_ERR_WORKSPACE),
+    (dict(wsb=8), B.SPEC_ERR_WORKSPACE),
+    (dict(ws=(1 << 26) + 4), B.SPEC_ERR_WORKSPACE),   # misaligned
+    (dict(T=1e-6), B.SPEC_ERR_UNSUPPORTED),
+])
+def test_sample_rejects_bad_arguments(L, kw, status):
+    assert _sample(L, **kw) == status
+    assert B.last_error()
+
+
+def test_empty_batch_is_a_no_op(L):
+    assert _sample(L, B=0, target=0, out=0, nacc=0, ws=0) == B.SPEC_OK
+    P = ctypes.c_void_p
+    assert L.spec_verify_greedy(None, 0, None, 0, 4, 100, None, None, None, 0, None) == B.SPEC_OK
+    assert L.spec_verify_tree_greedy(None, 0, None, None, 0, 3, 100, 2, None, None, None, None, 0, None) == B.SPEC_OK
+
+
+def test_greedy_and_tree_reject_bad_arguments(L):
+    P = ctypes.c_void_p
+    assert L.spec_verify_greedy(P(16), 0, P(32), 1, 40, 10, P(48), P(64), P(256), 1 << 20, None) == B.SPEC_ERR_INVALID_ARG
+    assert L.spec_verify_greedy(P(16), 0, P(32), 1, 4, 10, P(48), P(64), P(256), 4, None) == B.SPEC_ERR_WORKSPACE
+    tree = L.spec_verify_tree_greedy
+    assert tree(P(16), 0, P(32), P(48), 1, 2000, 10, 3, P(64), P(80), None, P(256), 1 << 20, None) == B.SPEC_ERR_INVALID_ARG
+    assert tree(P(16), 0, P(32), P(48), 1, 8, 10, 8, P(64), P(80), None, P(256), 1 << 20, None) == B.SPEC_ERR_INVALID_ARG
+    assert tree(P(16), 0, None, P(48), 1, 8, 10, 3, P(64), P(80), None, P(256), 1 << 20, None) == B.SPEC_ERR_INVALID_ARG
+
+
+def test_debug_residual_rejects_bad_position(L):
+    P = ctypes.c_void_p
+    f = L.spec_debug_residual
+    args = [P(16), 0, P(32), 0, 0, P(48), P(64), 1.0, 2, 3, 10]
+    assert f(*args, 2, 0, P(80), P(96), P(112), P(128), P(256), 1 << 20, None) == B.SPEC_ERR_INVALID_ARG
+    assert f(*args, 0, 4, P(80), P(96), P(112), P(128), P(256), 1 << 20, None) == B.SPEC_ERR_INVALID_ARG
+
+
+def test_status_strings(L):
+    assert B.status_string(0) == "SPEC_OK"
+    assert B.status_string(4) == "SPEC_ERR_WORKSPACE"
+    assert B.status_string(99) == "SPEC_ERR_UNKNOWN"
