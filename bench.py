@@ -232,18 +232,12 @@ def run_ours(args, ws, rank, local):
             import torch.distributed as dist
             dist.barrier()
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    # keep the GPU busy while the sampler starts (untimed)
-    t_end = time.time() + 0.5
-    while time.time() < t_end:
+    for _ in range(args.warmup):
         step()
-        torch.cuda.synchronize()
+    torch.cuda.synchronize()
 
     sv.spec_profile_begin(args.steps)
     barrier()

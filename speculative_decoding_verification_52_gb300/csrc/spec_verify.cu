@@ -21,6 +21,7 @@
 
 #include "common.cuh"
 #include "finish.cuh"
+#include "fused.cuh"
 #include "spec_verify.h"
 #include "sweep.cuh"
 
@@ -47,6 +48,8 @@ constexpr int kMaxDevices = 64;
 constexpr unsigned long long kWaitNs = 1000000000ull;   // bounded waits: 1 s
 
 int max_slices(int V) { return std::max(1, (V + kMinSlice - 1) / kMinSlice); }
+// residual slices of the fused sampling kernel are >= 8192 elements
+int max_rslices(int V) { return std::max(1, (V + 8191) / 8192); }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -280,20 +283,131 @@ int finish_max_cluster(int dev) {
   return mc[dev] > 0 ? mc[dev] : 8;
 }
 
+// Workspace of the fused sampling kernel:
+//   [FuCtl | cnt1[B] | cnt2[B] | queue[B*Sr]]  zeroed per call
+//   [info[B] | rsum[B*Sr] | part[rows*S]]
+struct FusedLayout {
+  size_t zero_bytes, info_off, rsum_off, part_off, total;
+};
+FusedLayout fused_layout(int B, int K, int V) {
+  FusedLayout l{};
+  const size_t sr = static_cast<size_t>(max_rslices(V));
+  l.zero_bytes = align_up(sizeof(FuCtl) + 8u * static_cast<size_t>(B) + 4u * static_cast<size_t>(B) * sr, 16);
+  l.info_off = l.zero_bytes;
+  l.rsum_off = align_up(l.info_off + sizeof(SeqInfo) * static_cast<size_t>(B), 16);
+  l.part_off = align_up(l.rsum_off + sizeof(double) * static_cast<size_t>(B) * sr, 16);
+  const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(2 * K + 1);
+  l.total = align_up(l.part_off + rows * static_cast<size_t>(max_slices(V)) * sizeof(float2), 256);
+  return l;
+}
+
+template <class TP, class TQ, bool PROBS>
+int fused_per_sm(int dev) {
+  static int per_sm[kMaxDevices];
+  auto kern = fused_sample_kernel<TP, TQ, PROBS>;
+  once_per_device(dev, [&] {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(fu_smem_bytes())) !=
+        cudaSuccess)
+      return false;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, FU_THREADS, fu_smem_bytes()) != cudaSuccess)
+      return false;
+    per_sm[dev] = std::max(1, n);
+    return true;
+  });
+  return per_sm[dev];
+}
+
+template <class TP, class TQ, bool PROBS>
+spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, const void* draft,
+                               const int32_t* tokens, const float* uni, float c, int B, int K, int V, int32_t* out,
+                               int32_t* nacc, void* ws, int debug_b, int debug_t, float* debug_row,
+                               float* debug_mass, cudaStream_t st) {
+  constexpr int QE = PROBS ? 4 : TQ::esz;
+  const int per_sm = fused_per_sm<TP, TQ, PROBS>(dev);
+  if (per_sm <= 0) return fail(SPEC_ERR_CUDA, "fused kernel setup failed: %s", cudaGetErrorString(cudaGetLastError()));
+  const int grid_cap = di.sms * per_sm;
+  const int RB = PROBS ? K + 1 : 2 * K + 1;
+  const long long rows = static_cast<long long>(B) * RB;
+  // sweep slices: ~48 KB units, but at least two units per CTA when the batch is small
+  const int smax = max_slices(V);
+  const long long row_bytes = static_cast<long long>(V) * std::max(TP::esz, QE);
+  int S = std::max(1, ceil_div(row_bytes, 49152));
+  S = std::max(S, static_cast<int>(std::min<long long>(smax, (2LL * grid_cap + rows - 1) / rows)));
+  S = std::min(S, smax);
+  int L = (ceil_div(V, S) + 7) / 8 * 8;
+  S = ceil_div(V, L);
+  const long long U = rows * S;
+  if (U >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "batch too large for one call");
+  const int RE = (TP::esz == 2 && QE == 2) ? 4096 : 2048;
+  const int Lr = 4 * RE;
+  const int Sr = ceil_div(V, Lr);
+  if (Sr > FU_MAX_SR || Sr > max_rslices(V)) return fail(SPEC_ERR_UNSUPPORTED, "V=%d too large", V);
+
+  const FusedLayout lay = fused_layout(B, K, V);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  FusedArgs a{};
+  a.target = static_cast<const unsigned char*>(target);
+  a.draft = static_cast<const unsigned char*>(draft);
+  a.tokens = tokens;
+  a.uni = uni;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.RB = RB;
+  a.S = S;
+  a.L = L;
+  a.Sr = Sr;
+  a.Lr = Lr;
+  a.RE = RE;
+  a.U = static_cast<unsigned>(U);
+  a.c = c;
+  a.ctl = reinterpret_cast<FuCtl*>(w);
+  a.cnt1 = reinterpret_cast<unsigned*>(w + sizeof(FuCtl));
+  a.cnt2 = a.cnt1 + B;
+  a.queue = a.cnt2 + B;
+  a.info = reinterpret_cast<SeqInfo*>(w + lay.info_off);
+  a.rsum = reinterpret_cast<double*>(w + lay.rsum_off);
+  a.part = reinterpret_cast<float2*>(w + lay.part_off);
+  a.out_tokens = out;
+  a.num_accepted = nacc;
+  a.debug_b = debug_b;
+  a.debug_t = debug_t;
+  a.debug_row = debug_row;
+  a.debug_mass = debug_mass;
+  a.timeout_ns = kWaitNs;
+  cudaError_t e = cudaMemsetAsync(ws, 0, lay.zero_bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace control reset");
+  prof_mark(0, st);
+  const long long work = U + static_cast<long long>(B) * Sr;
+  const int grid = static_cast<int>(std::min<long long>(grid_cap, work));
+  fused_sample_kernel<TP, TQ, PROBS><<<grid, FU_THREADS, fu_smem_bytes(), st>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "fused sampling launch");
+  prof_mark(1, st);
+  prof_mark(2, st);
+  return SPEC_OK;
+}
+
 template <class TP, class TQ, bool PROBS>
 spec_status_t run_sample(const DevInfo& di, int dev, const void* target, const void* draft, const int32_t* tokens,
                          const float* uni, float T, int B, int K, int V, int32_t* out, int32_t* nacc, void* ws,
                          int debug_b, int debug_t, float* debug_row, float* debug_mass, cudaStream_t st) {
   constexpr int QE = PROBS ? 4 : TQ::esz;
   const bool vec = aligned16(target) && (static_cast<long long>(V) * TP::esz) % 16 == 0 &&
-                   (K == 0 || (aligned16(draft) && (static_cast<long long>(V) * QE) % 16 == 0));
+                   (K == 0 || (aligned16(draft) && (static_cast<long long>(V) * QE) % 16 == 0)) && V % 8 == 0;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+  if (vec)
+    return run_sample_fused<TP, TQ, PROBS>(di, dev, target, draft, tokens, uni, c, B, K, V, out, nacc, ws, debug_b,
+                                           debug_t, debug_row, debug_mass, st);
+
+  // scalar path for unaligned rows: sweep kernel + clustered finishing kernel
   const long long rows0 = static_cast<long long>(B) * (K + 1);
   const long long rows1 = PROBS ? 0 : static_cast<long long>(B) * K;
   float2* part = reinterpret_cast<float2*>(ws);
   prof_mark(0, st);
   int S = 0;
-  spec_status_t s = launch_sweep<TP, TQ, MODE_STATS>(di, dev, vec, static_cast<const unsigned char*>(target), rows0,
+  spec_status_t s = launch_sweep<TP, TQ, MODE_STATS>(di, dev, false, static_cast<const unsigned char*>(target), rows0,
                                                      static_cast<const unsigned char*>(draft), rows1, V, c, part, st, S);
   if (s != SPEC_OK) return s;
   prof_mark(1, st);
@@ -316,7 +430,7 @@ spec_status_t run_sample(const DevInfo& di, int dev, const void* target, const v
   a.debug_row = debug_row;
   a.debug_mass = debug_mass;
 
-  const int maxcl = vec ? finish_max_cluster<TP, TQ, PROBS, true>(dev) : finish_max_cluster<TP, TQ, PROBS, false>(dev);
+  const int maxcl = finish_max_cluster<TP, TQ, PROBS, false>(dev);
   int CL = std::min(maxcl, std::max(1, ceil_div(V, 8192)));
   int L = (ceil_div(V, CL) + 7) / 8 * 8;
   while (L > FS_MAX_L && CL < maxcl) {
@@ -325,8 +439,7 @@ spec_status_t run_sample(const DevInfo& di, int dev, const void* target, const v
   }
   if (L > FS_MAX_L) return fail(SPEC_ERR_UNSUPPORTED, "V=%d exceeds the sampling limit (%d)", V, FS_MAX_L * maxcl);
   a.L = L;
-  s = vec ? launch_finish_sample<TP, TQ, PROBS, true>(di, dev, a, CL, st)
-          : launch_finish_sample<TP, TQ, PROBS, false>(di, dev, a, CL, st);
+  s = launch_finish_sample<TP, TQ, PROBS, false>(di, dev, a, CL, st);
   if (s != SPEC_OK) return s;
   prof_mark(2, st);
   return SPEC_OK;
@@ -408,7 +521,8 @@ extern "C" {
 size_t spec_workspace_bytes(int B, int K, int V) {
   if (B < 0 || K < 0 || K > SPEC_MAX_K || V < 1) return 0;
   const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(2 * K + 1);
-  return align_up(rows * static_cast<size_t>(max_slices(V)) * sizeof(float2), 256);
+  const size_t plain = align_up(rows * static_cast<size_t>(max_slices(V)) * sizeof(float2), 256);
+  return std::max(plain, fused_layout(B, K, V).total);
 }
 
 size_t spec_tree_workspace_bytes(int B, int N, int V) {

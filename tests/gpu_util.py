@@ -40,14 +40,15 @@ def oracle_sample(orc, batch, T=None):
                              batch.draft_tokens, batch.uniforms, T)
 
 
-def compare_sample(out, n, ref):
+def compare_sample(out, n, ref, stats=None):
     """Bit-exact comparison except after decisions the oracle flags as within
     1e-6 of flipping: a near accept test at t excludes slots >= t and the
     accept count; a near CDF boundary excludes only the drawn token.
-    Returns the number of flagged sequences; asserts on any other mismatch."""
+    Returns the number of flagged sequences; asserts on any other mismatch.
+    `stats` (a dict) receives flagged / flagged_mismatch counts."""
     na, nc = ref["near_accept"], ref["near_cdf"]
     ro, rn = ref["out_tokens"], ref["num_accepted"]
-    flagged = 0
+    flagged = flagged_mismatch = 0
     bad = []
     for b in range(len(rn)):
         if na[b] >= 0:
@@ -55,15 +56,21 @@ def compare_sample(out, n, ref):
             t = na[b]
             if not (out[b, :t] == ro[b, :t]).all():
                 bad.append(b)
+            if n[b] != rn[b] or not (out[b] == ro[b]).all():
+                flagged_mismatch += 1
             continue
         if nc[b]:
             flagged += 1
             m = rn[b]
             if n[b] != m or not (out[b, :m] == ro[b, :m]).all() or not (out[b, m + 1:] == ro[b, m + 1:]).all():
                 bad.append(b)
+            if out[b, m] != ro[b, m]:
+                flagged_mismatch += 1
             continue
         if n[b] != rn[b] or not (out[b] == ro[b]).all():
             bad.append(b)
     assert not bad, f"{len(bad)} sequences differ from the oracle, first {bad[:5]}: " \
                     f"gpu n={n[bad[0]]} {out[bad[0]].tolist()} oracle n={rn[bad[0]]} {ro[bad[0]].tolist()}"
+    if stats is not None:
+        stats.update(flagged=flagged, flagged_mismatch=flagged_mismatch, total=len(rn))
     return flagged

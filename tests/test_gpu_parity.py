@@ -129,8 +129,13 @@ def test_sample_headline_full(orc):
     b = gen.config_headline()
     ref = gu.oracle_sample(orc, b)
     out, n = gu.gpu_sample(b)
-    flagged = gu.compare_sample(out, n, ref)
-    assert flagged <= 2
+    st = {}
+    gu.compare_sample(out, n, ref, st)
+    # at V = 128256 a token's residual mass is ~1e-5 of the total, so about one
+    # draw in ten lands within 1e-6 of a CDF boundary; nearly all still agree
+    print("headline flagged:", st)
+    assert st["flagged"] < 0.25 * b.B
+    assert st["flagged_mismatch"] <= 2
     acc = (n.astype(np.float64)).mean() / b.K
     assert 0.4 < acc < 0.95
 
