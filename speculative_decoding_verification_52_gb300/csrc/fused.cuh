@@ -643,6 +643,8 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
       d.flags = FL_FIRST | FL_LAST;
       d.status = inf.status;
       mbar_arrive(&sh.full[stage]);
+      // the stage was released, so its previous copy has landed: nothing to drain
+      last_parity[stage] = -1;
       advance();
       continue;
     }
@@ -679,11 +681,16 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
   if (next_stage()) {
     sh.desc[stage].kind = KIND_STOP;
     mbar_arrive(&sh.full[stage]);
+    last_parity[stage] = -1;
   }
-  // do not leave while a copy may still land in this CTA's shared memory
+  // Do not leave while a copy may still land in this CTA's shared memory.  A
+  // stage's recorded parity is that of its last copy; any later arrival on the
+  // stage (which would flip the phase again) clears the record, so a wait here
+  // can only be for a copy that has not been consumed yet (abort path).
 #pragma unroll
   for (int s = 0; s < FU_NSTAGE; ++s)
-    if (last_parity[s] >= 0) mbar_wait(&sh.full[s], static_cast<uint32_t>(last_parity[s]), a.timeout_ns);
+    if (last_parity[s] >= 0 && !mbar_wait(&sh.full[s], static_cast<uint32_t>(last_parity[s]), a.timeout_ns))
+      atomicOr(&a.ctl->err, 8u);
 }
 
 // ---------------------------------------------------------------------------

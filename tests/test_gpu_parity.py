@@ -322,6 +322,25 @@ def test_tree_bad_topology_and_nan(orc):
     assert rn.tolist() == [3, 3, -1]
 
 
+def test_calls_finish_without_hitting_wait_bounds():
+    """Every wait in the kernels is bounded (1 s); a call that silently ran into
+    a bound would still be correct but slow.  The headline-sized call must take
+    milliseconds, repeatedly."""
+    import time
+    b = gen.config_headline(seqs=list(range(64)))
+    tgt, dft = gu.dev_tensor(b.target, b.dtype), gu.dev_tensor(b.draft, b.dtype)
+    tok, uni = gu.i32(b.draft_tokens), gu.f32(b.uniforms)
+    sv.spec_verify_sample(tgt, dft, tok, uni, b.T)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(5):
+        _, n = sv.spec_verify_sample(tgt, dft, tok, uni, b.T)
+        sv.spec_verify_greedy(tgt, tok)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 0.5
+    assert (n.cpu().numpy() >= 0).all()
+
+
 def test_non_default_stream(orc):
     b = gen.config_zipf(T=1.0, B=16, V=8192)
     s = torch.cuda.Stream()
