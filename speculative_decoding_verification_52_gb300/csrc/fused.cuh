@@ -3,30 +3,34 @@
 // exactness rule"; "Speculative decoding: draft, verify, repeat", steps 1-3;
 // "Speculative Decoding: from idea to SOTA", section 3).
 //
-// Work items, handed out dynamically (global atomic counters) to a grid of
-// SMs x 3 CTAs:
-//   sweep unit    (sequence b, row r, slice j): softmax-normaliser partial
+// Work items:
+//   sweep unit    (sequence b, row r, slice j): softmax-normaliser partials
 //                 (max m, sum 2^(z*c - fl(m*c))) of one slice of one target or
-//                 draft row.  Units are numbered sequence-major, so a sequence's
-//                 units run at about the same time.
-//   residual unit (sequence b, slice j): sum over one slice of the stopping
-//                 row pair of w = max(0, p - q) (or p alone for the bonus row).
-// Whichever CTA completes the last sweep unit of a sequence runs the accept
-// scan for it (merging the partials in double precision), writes the accepted
-// prefix, and publishes the sequence's residual units in a queue; producers
-// take queued residual units before new sweep units, so the stopping rows are
-// re-read while they are still in L2.  Whichever CTA completes the last
-// residual unit of a sequence runs the inverse-CDF pick: it finds the slice
-// holding u*R from the slice sums, re-reads that slice, and locates the token
-// with a block-wide prefix scan.
-//
-// Inside a CTA: one producer thread streams each work item's bytes into a
-// 4-stage ring of 16 KB shared-memory stages with 1-D bulk async copies
-// (cp.async.bulk, completion on an mbarrier per stage) and writes a small
-// descriptor per stage; eight consumer warps do the arithmetic.  Every wait
-// (stage barriers, the consumer-group barrier, queue polling) is bounded in
-// time; a timeout sets an error word and the last CTA to leave marks every
-// sequence -2.
+//                 draft row.  Units are numbered sequence-major and dealt to the
+//                 CTAs round-robin (no atomics), so the batch is swept roughly
+//                 in sequence order and sequences complete one after another.
+//   residual unit (sequence b, slice j): sum over one slice of the stopping row
+//                 pair of w = max(0, p - q) (p alone for the bonus row).
+// Roles inside a CTA (one warp each, plus eight consumer warps):
+//   producer   one thread streams work-item bytes into a 4-stage ring of 16 KB
+//              shared-memory stages with 1-D bulk async copies (cp.async.bulk,
+//              completion counted on an mbarrier per stage) and writes a small
+//              descriptor per stage.  It takes published residual units before
+//              its next sweep unit, so stopping rows are re-read from L2.
+//   consumers  each of the eight warps reduces its share of every stage, writes
+//              its own partial at the end of a work item and counts it in the
+//              sequence's arrival counter; no CTA-wide barrier is involved.
+//              The warp whose arrival completes a sequence hands a task to the
+//              finisher warp through a shared-memory queue.
+//   finisher   runs the accept scan of a sequence whose sweep is complete
+//              (warp-parallel merge of the partials, one lane per position),
+//              writes the accepted prefix and publishes the residual units; and
+//              runs the inverse-CDF pick of a sequence whose residual sums are
+//              complete (slice prefix sums, then a warp-wide prefix scan over
+//              the chosen slice, re-read from L2).
+// Every wait (stage barriers, the task queue, residual-queue polling) is
+// bounded in time; a timeout sets an error word, and the last CTA to leave then
+// marks every sequence -2.
 #pragma once
 
 #include <type_traits>
@@ -35,13 +39,14 @@
 
 namespace sv {
 
-constexpr int FU_CW = 8;
+constexpr int FU_CW = 8;                          // consumer warps
 constexpr int FU_CT = FU_CW * 32;
-constexpr int FU_THREADS = FU_CT + 32;
+constexpr int FU_THREADS = FU_CT + 64;            // + producer warp + finisher warp
+constexpr int FU_FIN_WARP = FU_CW + 1;
 constexpr int FU_STAGE = 16384;
 constexpr int FU_NSTAGE = 4;
-constexpr int FU_MAX_ROWS = 2 * 31 + 1;
-constexpr int FU_MAX_SR = 64;
+constexpr int FU_MAX_SR = 64;                     // residual slices per row (host checks)
+constexpr int FU_TASKQ = 64;                      // finisher task queue capacity
 
 enum : int { KIND_STOP = -1, KIND_SWEEP = 0, KIND_RESID = 1 };
 enum : int { FL_FIRST = 1, FL_LAST = 2, FL_DRAFT = 4, FL_HASQ = 8 };
@@ -54,17 +59,15 @@ struct SeqInfo {          // per sequence, written by the accept scan
   float pad;
 };
 
-struct FuCtl {            // zeroed before every call
-  unsigned next;          // sweep units claimed
-  unsigned rnext;         // residual units claimed
-  unsigned rres;          // residual units reserved by finished scans
-  unsigned err;           // a wait timed out
-  unsigned done;          // CTAs that have left
-  unsigned pad[3];
+struct FuCtl {                    // zeroed before every call (32 bytes reserved)
+  unsigned long long rq;          // residual queue: low 32 bits reserved, high 32 bits claimed
+  unsigned err;                   // a wait timed out
+  unsigned done;                  // CTAs that have left
 };
+static_assert(sizeof(FuCtl) <= 32, "control block must fit its 32-byte slot");
 
 struct StageDesc {
-  int kind, b, unit, e0, n, flags, status, tstar;
+  int kind, b, unit, e0, n, flags, tstar, pad;
   float AP, AQ, iSp, iSq;
 };
 
@@ -79,12 +82,12 @@ struct FusedArgs {
   unsigned U;                    // sweep units = B * RB * S
   float c;                       // log2(e) / T
   FuCtl* ctl;
-  unsigned* cnt1;                // [B] sweep units completed
-  unsigned* cnt2;                // [B] residual units completed
+  unsigned* cnt1;                // [B] sweep warp-partials completed
+  unsigned* cnt2;                // [B] residual warp-partials completed
   unsigned* queue;               // [B * Sr] residual units: b * FU_MAX_SR + j + 1
   SeqInfo* info;                 // [B]
-  double* rsum;                  // [B * Sr] residual slice sums
-  float2* part;                  // [U] sweep partials
+  double* rpart;                 // [B * Sr * FU_CW] residual warp-partial sums
+  float2* part;                  // [U * FU_CW] sweep warp-partials
   int32_t* out_tokens;           // [B, K+1]
   int32_t* num_accepted;         // [B]
   int debug_b, debug_t;
@@ -96,68 +99,58 @@ struct FusedArgs {
 struct FuShared {
   uint64_t full[FU_NSTAGE];
   uint64_t empty[FU_NSTAGE];
-  uint64_t gbar;                 // consumer-group barrier (one arrival per consumer warp)
   StageDesc desc[FU_NSTAGE];
-  float2 red2[FU_CW];
-  double redd[FU_CW];
-  double wsum[FU_CW];
-  int flag_last;
+  int task[FU_TASKQ];            // (b << 1 | kind) + 1, 0 = empty slot
+  unsigned task_tail;            // next slot to fill (shared-memory atomics)
+  int cons_done;                 // consumer warps that have left
   int abort;
-  int pick, lastpos;
-  // accept scan
-  float rowA[FU_MAX_ROWS];
-  double rowS[FU_MAX_ROWS];
-  int rowState[FU_MAX_ROWS];
-  float gp[32], gq[32], u0[32];
-  int xt[32];
-  // pick
-  double sl[FU_MAX_SR];
-  double base, target, R;
-  int jstar, mode;
-  SeqInfo inf;
 };
 
 __device__ __forceinline__ bool fu_aborted(const FuShared& sh) {
   return *reinterpret_cast<const volatile int*>(&sh.abort) != 0;
 }
-__device__ __forceinline__ void fu_set_abort(FuShared& sh) { *reinterpret_cast<volatile int*>(&sh.abort) = 1; }
+__device__ __forceinline__ void fu_fail(FuShared& sh, FuCtl* ctl, unsigned bit) {
+  *reinterpret_cast<volatile int*>(&sh.abort) = 1;
+  atomicOr(&ctl->err, bit);
+}
 
 // element loaders for 8 consecutive elements (16 B of bf16, 32 B of f32)
 template <class T>
-__device__ __forceinline__ void load8(const unsigned char* p, float* x);
-template <>
-__device__ __forceinline__ void load8<BF16T>(const unsigned char* p, float* x) {
-  const uint4 q = *reinterpret_cast<const uint4*>(p);
-  BF16T::unpack(q, x);
-}
-template <>
-__device__ __forceinline__ void load8<F32T>(const unsigned char* p, float* x) {
-  const uint4 q0 = reinterpret_cast<const uint4*>(p)[0];
-  const uint4 q1 = reinterpret_cast<const uint4*>(p)[1];
-  F32T::unpack(q0, x);
-  F32T::unpack(q1, x + 4);
+__device__ __forceinline__ void load8_smem(const unsigned char* p, float* x) {
+  if constexpr (T::esz == 2) {
+    BF16T::unpack(*reinterpret_cast<const uint4*>(p), x);
+  } else {
+    F32T::unpack(reinterpret_cast<const uint4*>(p)[0], x);
+    F32T::unpack(reinterpret_cast<const uint4*>(p)[1], x + 4);
+  }
 }
 template <class T>
 __device__ __forceinline__ void load8_global(const unsigned char* p, float* x) {
   if constexpr (T::esz == 2) {
-    const uint4 q = __ldcg(reinterpret_cast<const uint4*>(p));
-    BF16T::unpack(q, x);
+    BF16T::unpack(__ldcg(reinterpret_cast<const uint4*>(p)), x);
   } else {
-    const uint4 q0 = __ldcg(reinterpret_cast<const uint4*>(p));
-    const uint4 q1 = __ldcg(reinterpret_cast<const uint4*>(p) + 1);
-    F32T::unpack(q0, x);
-    F32T::unpack(q1, x + 4);
+    F32T::unpack(__ldcg(reinterpret_cast<const uint4*>(p)), x);
+    F32T::unpack(__ldcg(reinterpret_cast<const uint4*>(p) + 1), x + 4);
   }
 }
 
-// residual weight of one element, identical arithmetic in the slice sums and
-// in the pick (so both see the same fp32 values)
+// residual weight of one element; the slice sums and the pick use exactly this
+// arithmetic, so both see the same fp32 values
 __device__ __forceinline__ float resid_w(float zp, float zq, float c, float nAP, float nAQ, float iSp, float iSq,
                                          bool has_q, bool probs) {
   const float wp = __fmul_rn(ex2_approx(__fmaf_rn(zp, c, nAP)), iSp);
   if (!has_q) return wp;
   const float eq = probs ? zq : ex2_approx(__fmaf_rn(zq, c, nAQ));
   return fmaxf(0.f, __fmaf_rn(-eq, iSq, wp));
+}
+
+// 2^x for a double x <= 0 with ~1e-7 relative accuracy, without a double
+// exp2: the accurate fp32 exp2f of the leading part, corrected to first order
+// for the remainder
+__device__ __forceinline__ double exp2_d(double x) {
+  const float xf = static_cast<float>(x);
+  const double r = x - static_cast<double>(xf);
+  return static_cast<double>(exp2f(xf)) * (1.0 + r * 0.6931471805599453);
 }
 
 // ---------------------------------------------------------------------------
@@ -244,17 +237,14 @@ __device__ __forceinline__ void stats_stage(const uint4* buf, int nvec, int ctid
 // residual partial sum over one stage: P chunk at buf, Q chunk at buf + RE*esz_P
 template <class TP, class TQ, bool PROBS>
 __device__ __forceinline__ float resid_stage(const unsigned char* buf, const StageDesc& d, int RE, int ctid, float c) {
-  constexpr int QE = PROBS ? 4 : TQ::esz;
+  using QT = typename std::conditional<PROBS, F32T, TQ>::type;
   const bool has_q = d.flags & FL_HASQ;
   const unsigned char* qb = buf + RE * TP::esz;
   float acc = 0.f;
   for (int g = ctid; g < d.n / 8; g += FU_CT) {
     float zp[8], zq[8];
-    load8<TP>(buf + g * 8 * TP::esz, zp);
-    if (has_q) {
-      if constexpr (PROBS || QE == 4) load8<F32T>(qb + g * 8 * 4, zq);
-      else load8<BF16T>(qb + g * 8 * 2, zq);
-    }
+    load8_smem<TP>(buf + g * 8 * TP::esz, zp);
+    if (has_q) load8_smem<QT>(qb + g * 8 * QT::esz, zq);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       acc += resid_w(zp[i], has_q ? zq[i] : 0.f, c, -d.AP, -d.AQ, d.iSp, d.iSq, has_q, PROBS);
@@ -262,171 +252,180 @@ __device__ __forceinline__ float resid_stage(const unsigned char* buf, const Sta
   return acc;
 }
 
-// ---------------------------------------------------------------------------
-// consumer-group barrier on an mbarrier (bounded wait)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ bool group_sync(FuShared& sh, uint32_t& gphase, uint64_t timeout) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.gbar);
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(&sh.gbar, gphase, timeout));
-  gphase ^= 1u;
-  if (!ok) fu_set_abort(sh);
-  return __all_sync(0xffffffffu, ok && !fu_aborted(sh));
+// value of row r held by lanes (row r lives in lane r & 31, register r >> 5)
+template <class T>
+__device__ __forceinline__ T row_get(const T (&v)[2], int r) {
+  const T v0 = __shfl_sync(0xffffffffu, v[0], r & 31);
+  const T v1 = __shfl_sync(0xffffffffu, v[1], r & 31);
+  return r < 32 ? v0 : v1;
 }
 
 // ---------------------------------------------------------------------------
-// accept scan of sequence b (all consumer threads)
+// finisher: accept scan of sequence b (one warp)
 // ---------------------------------------------------------------------------
 template <class TP, class TQ, bool PROBS>
-__device__ bool finish_scan(const FusedArgs& a, FuShared& sh, int b, int ctid, uint32_t& gphase) {
+__device__ void finish_scan(const FusedArgs& a, int b, int lane) {
   const int K = a.K, W = K + 1, V = a.V;
-  if (ctid < a.RB) {
-    // merge the S slice partials of row ctid (double precision, offsets fl(m*c))
-    const float2* part = a.part + (static_cast<long long>(b) * a.RB + ctid) * a.S;
+  const int npart = a.S * FU_CW;
+  // lane owns rows lane and lane + 32: merge their S x 8 warp partials
+  float Ar[2] = {0.f, 0.f};
+  double Sr[2] = {0.0, 0.0};
+  int st[2] = {1, 1};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = lane + 32 * h;
+    if (r >= a.RB) continue;
+    const float2* part = a.part + (static_cast<long long>(b) * a.RB + r) * npart;
     float M = kNegInf;
     bool poison = false;
-    for (int j = 0; j < a.S; ++j) {
-      const float2 p = __ldcg(part + j);
+    for (int i = 0; i < npart; ++i) {
+      const float2 p = __ldcg(part + i);
       if (p.x != p.x) poison = true;
       else M = fmaxf(M, p.x);
     }
-    int st = 0;
-    double Sr = 0.0;
-    float AM = 0.f;
-    if (poison) st = 2;
-    else if (M == kNegInf) st = 1;
-    else {
-      AM = __fmul_rn(M, a.c);
-      for (int j = 0; j < a.S; ++j) {
-        const float2 p = __ldcg(part + j);
-        if (p.x == kNegInf) continue;
-        Sr += static_cast<double>(p.y) * exp2(static_cast<double>(__fmul_rn(p.x, a.c)) - static_cast<double>(AM));
-      }
-      st = (isfinite(Sr) && Sr > 0.0) ? 0 : 1;
+    if (poison) { st[h] = 2; continue; }
+    if (M == kNegInf) { st[h] = 1; continue; }
+    const float AM = __fmul_rn(M, a.c);
+    double acc = 0.0;
+    for (int i = 0; i < npart; ++i) {
+      const float2 p = __ldcg(part + i);
+      if (p.x == kNegInf) continue;
+      // fl(m*c) - fl(M*c) is exact in fp32 whenever the factor is not negligible
+      acc += static_cast<double>(p.y) * static_cast<double>(exp2f(__fmul_rn(p.x, a.c) - AM));
     }
-    sh.rowA[ctid] = AM;
-    sh.rowS[ctid] = Sr;
-    sh.rowState[ctid] = st;
-  } else if (ctid >= 64 && ctid < 64 + K) {
-    const int t = ctid - 64;
-    const int x = a.tokens[static_cast<long long>(b) * K + t];
-    sh.xt[t] = x;
-    if (x >= 0 && x < V) {
-      sh.gp[t] = TP::load(a.target, (static_cast<long long>(b) * W + t) * V + x);
-      const long long oq = (static_cast<long long>(b) * K + t) * V + x;
-      sh.gq[t] = PROBS ? F32T::load(a.draft, oq) : TQ::load(a.draft, oq);
-    }
-    sh.u0[t] = a.uni[(static_cast<long long>(b) * W + t) * 2];
+    Ar[h] = AM;
+    Sr[h] = acc;
+    st[h] = (isfinite(acc) && acc > 0.0) ? 0 : 1;
   }
-  if (!group_sync(sh, gphase, a.timeout_ns)) return false;
-  if (ctid == 0) {
-    int status = 0, tstar = K;
-    for (int t = 0; t < K; ++t)
-      if (sh.xt[t] < 0 || sh.xt[t] >= V) status = -1;
-    const bool forced = (b == a.debug_b);
-    const double cd = static_cast<double>(a.c);
-    for (int t = 0; status == 0 && !forced && t < K; ++t) {
-      if (sh.rowState[t] != 0) { status = sh.rowState[t] == 2 ? -2 : -1; break; }
-      const double pa = exp2(static_cast<double>(sh.gp[t]) * cd - static_cast<double>(sh.rowA[t])) / sh.rowS[t];
+
+  // lane t tests position t
+  const int t = lane;
+  const int rp = t < W ? t : 0;
+  const int rq = (t < K && !PROBS) ? W + t : 0;
+  const float At = row_get(Ar, rp), Aq = row_get(Ar, rq);
+  const double St = row_get(Sr, rp), Sq = row_get(Sr, rq);
+  const int stt = row_get(st, rp), stq = row_get(st, rq);
+  int x = -1;
+  bool tok_bad = false, acc_t = true;
+  int row_bad = 0;   // 0 ok, 1 invalid, 2 poisoned (rows read at position t)
+  if (t < K) {
+    x = a.tokens[static_cast<long long>(b) * K + t];
+    tok_bad = x < 0 || x >= V;
+    row_bad = stt;
+    if (!PROBS && row_bad == 0) row_bad = stq;
+    if (!tok_bad && row_bad == 0) {
+      const double cd = static_cast<double>(a.c);
+      const double zp = static_cast<double>(TP::load(a.target, (static_cast<long long>(b) * W + t) * V + x));
+      const double pa = exp2_d(zp * cd - static_cast<double>(At)) / St;
       double qc;
+      const long long oq = (static_cast<long long>(b) * K + t) * V + x;
       if (PROBS) {
-        const float qv = sh.gq[t];
-        if (qv != qv || qv < 0.f) { status = -1; break; }
+        const float qv = F32T::load(a.draft, oq);
+        if (qv != qv || qv < 0.f) row_bad = 1;
         qc = static_cast<double>(qv);
       } else {
-        const int r = W + t;
-        if (sh.rowState[r] != 0) { status = sh.rowState[r] == 2 ? -2 : -1; break; }
-        qc = exp2(static_cast<double>(sh.gq[t]) * cd - static_cast<double>(sh.rowA[r])) / sh.rowS[r];
+        const double zq = static_cast<double>(TQ::load(a.draft, oq));
+        qc = exp2_d(zq * cd - static_cast<double>(Aq)) / Sq;
       }
-      const bool accept = (qc == 0.0) || (static_cast<double>(sh.u0[t]) < pa / qc);
-      if (!accept) { tstar = t; break; }
+      const double u = static_cast<double>(a.uni[(static_cast<long long>(b) * W + t) * 2]);
+      acc_t = (qc == 0.0) || (u < pa / qc);
     }
-    if (forced) tstar = a.debug_t;
-    if (status == 0 && sh.rowState[tstar] != 0) status = sh.rowState[tstar] == 2 ? -2 : -1;
-    if (status == 0 && tstar < K && !PROBS && sh.rowState[W + tstar] != 0)
-      status = sh.rowState[W + tstar] == 2 ? -2 : -1;
+  }
+  const unsigned badtok = __ballot_sync(0xffffffffu, t < K && tok_bad);
+  // the scan stops at the first rejection or at the first position whose rows are bad
+  const unsigned stop = __ballot_sync(0xffffffffu, t < K && (row_bad != 0 || !acc_t));
+  int tstar = stop ? (__ffs(stop) - 1) : K;
+  const int rb_at = __shfl_sync(0xffffffffu, row_bad, tstar & 31);
+  int status = badtok ? -1 : 0;
+  if (b == a.debug_b) {
+    tstar = a.debug_t;
+  } else if (status == 0 && tstar < K && rb_at != 0) {
+    status = rb_at == 2 ? -2 : -1;
+  }
+  // the replacement draw reads the stopping rows
+  const int sp_state = row_get(st, tstar);
+  if (status == 0 && sp_state != 0) status = sp_state == 2 ? -2 : -1;
+  const bool has_q = tstar < K && !PROBS;
+  const int sq_state = row_get(st, has_q ? W + tstar : 0);
+  if (status == 0 && has_q && sq_state != 0) status = sq_state == 2 ? -2 : -1;
+  const float Ap = row_get(Ar, tstar);
+  const double Sp = row_get(Sr, tstar);
+  const float Aq2 = row_get(Ar, has_q ? W + tstar : 0);
+  const double Sq2 = row_get(Sr, has_q ? W + tstar : 0);
+
+  int32_t* out = a.out_tokens + static_cast<long long>(b) * W;
+  for (int j = lane; j < W; j += 32) {
+    const int xj = (j < K) ? a.tokens[static_cast<long long>(b) * K + j] : -1;
+    out[j] = (status == 0 && j < tstar) ? xj : -1;
+  }
+  if (lane == 0) {
+    a.num_accepted[b] = status == 0 ? tstar : status;
     SeqInfo inf;
     inf.status = status;
     inf.tstar = tstar;
-    inf.AP = sh.rowA[tstar];
-    inf.iSp = static_cast<float>(1.0 / sh.rowS[tstar]);
-    const bool has_q = tstar < K;
-    inf.AQ = (has_q && !PROBS) ? sh.rowA[W + tstar] : 0.f;
-    inf.iSq = (has_q && !PROBS) ? static_cast<float>(1.0 / sh.rowS[W + tstar]) : 1.f;
+    inf.AP = Ap;
+    inf.AQ = has_q ? Aq2 : 0.f;
+    inf.iSp = static_cast<float>(1.0 / Sp);
+    inf.iSq = has_q ? static_cast<float>(1.0 / Sq2) : 1.f;
     inf.u1 = a.uni[(static_cast<long long>(b) * W + tstar) * 2 + 1];
     inf.pad = 0.f;
-    int32_t* out = a.out_tokens + static_cast<long long>(b) * W;
-    for (int j = 0; j < W; ++j) out[j] = (status == 0 && j < tstar) ? sh.xt[j] : -1;
-    a.num_accepted[b] = status == 0 ? tstar : status;
     a.info[b] = inf;
-    __threadfence();
-    const unsigned k0 = atomicAdd(&a.ctl->rres, static_cast<unsigned>(a.Sr));
-    for (int j = 0; j < a.Sr; ++j) st_release_u32(a.queue + k0 + j, static_cast<unsigned>(b * FU_MAX_SR + j + 1));
   }
-  return group_sync(sh, gphase, a.timeout_ns);
+  __syncwarp();
+  __threadfence();
+  unsigned k0 = 0;
+  if (lane == 0) k0 = static_cast<unsigned>(atomicAdd(&a.ctl->rq, static_cast<unsigned long long>(a.Sr)));
+  k0 = __shfl_sync(0xffffffffu, k0, 0);
+  for (int j = lane; j < a.Sr; j += 32) st_release_u32(a.queue + k0 + j, static_cast<unsigned>(b * FU_MAX_SR + j + 1));
 }
 
 // ---------------------------------------------------------------------------
-// inverse-CDF pick of sequence b (all consumer threads)
+// finisher: inverse-CDF pick of sequence b (one warp)
 // ---------------------------------------------------------------------------
 template <class TP, class TQ, bool PROBS>
-__device__ bool finish_pick(const FusedArgs& a, FuShared& sh, int b, int ctid, uint32_t& gphase) {
-  constexpr int QE = PROBS ? 4 : TQ::esz;
+__device__ void finish_pick(const FusedArgs& a, int b, int lane) {
+  using QT = typename std::conditional<PROBS, F32T, TQ>::type;
   const int K = a.K, W = K + 1, V = a.V;
-  const int lane = ctid & 31, warp = ctid >> 5;
-  if (ctid == 0) {
-    SeqInfo inf;
+  SeqInfo inf;
+  {
     const int* src = reinterpret_cast<const int*>(a.info + b);
     int* dst = reinterpret_cast<int*>(&inf);
 #pragma unroll
     for (int i = 0; i < 8; ++i) dst[i] = __ldcg(src + i);
-    sh.inf = inf;
   }
-  if (ctid < a.Sr) sh.sl[ctid] = __ldcg(a.rsum + static_cast<long long>(b) * a.Sr + ctid);
-  if (!group_sync(sh, gphase, a.timeout_ns)) return false;
-  const SeqInfo inf = sh.inf;
-  if (inf.status != 0) return true;   // outputs already written by the scan
+  if (inf.status != 0) return;   // outputs already written by the scan
   const bool has_q0 = inf.tstar < K;
   const unsigned char* prow = a.target + (static_cast<long long>(b) * W + inf.tstar) * V * TP::esz;
-  const unsigned char* qrow = has_q0 ? a.draft + (static_cast<long long>(b) * K + inf.tstar) * V * QE : nullptr;
+  const unsigned char* qrow = has_q0 ? a.draft + (static_cast<long long>(b) * K + inf.tstar) * V * QT::esz : nullptr;
   const float c = a.c;
-
-  // residual mass zero: recompute the slice sums for w = p (rare)
-  bool has_q = has_q0;
-  for (int pass = 0; pass < 2; ++pass) {
-    if (ctid == 0) {
-      double R = 0.0;
-      for (int j = 0; j < a.Sr; ++j) R += sh.sl[j];
-      sh.R = R;
-      sh.mode = (R > 0.0 || !has_q) ? 0 : 1;
-      const double target = static_cast<double>(inf.u1) * R;
-      int js = -1, jlast = -1;
-      double pre = 0.0, base = 0.0;
-      for (int j = 0; j < a.Sr; ++j) {
-        if (sh.sl[j] > 0.0) {
-          jlast = j;
-          if (js < 0 && pre + sh.sl[j] > target) { js = j; base = pre; }
-        }
-        pre += sh.sl[j];
-      }
-      if (js < 0) {  // rounding: fall back to the last slice with mass
-        js = jlast;
-        base = 0.0;
-        for (int j = 0; j < jlast; ++j) base += sh.sl[j];
-      }
-      sh.jstar = js;
-      sh.base = base;
-      sh.target = target;
-      sh.pick = 0x7fffffff;
-      sh.lastpos = -1;
+  // slice sums (lanes own slices lane and lane + 32)
+  double sl[2] = {0.0, 0.0};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = lane + 32 * h;
+    if (j < a.Sr) {
+      const double* rp = a.rpart + (static_cast<long long>(b) * a.Sr + j) * FU_CW;
+      double s = 0.0;
+#pragma unroll
+      for (int w = 0; w < FU_CW; ++w) s += __ldcg(rp + w);
+      sl[h] = s;
     }
-    if (!group_sync(sh, gphase, a.timeout_ns)) return false;
-    if (sh.mode == 0) break;
+  }
+  bool has_q = has_q0;
+  double R = 0.0;
+  for (int pass = 0; pass < 2; ++pass) {
+    double tot = sl[0] + sl[1];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    R = tot;
+    if (R > 0.0 || !has_q) break;
+    // residual mass zero: draw from p_t instead (recompute the slice sums)
     has_q = false;
+    sl[0] = sl[1] = 0.0;
     for (int j = 0; j < a.Sr; ++j) {
       const int e0 = j * a.Lr, e1 = min(V, e0 + a.Lr);
       float acc = 0.f;
-      for (int g = e0 / 8 + ctid; g < e1 / 8; g += FU_CT) {
+      for (int g = e0 / 8 + lane; g < e1 / 8; g += 32) {
         float zp[8];
         load8_global<TP>(prow + static_cast<long long>(g) * 8 * TP::esz, zp);
 #pragma unroll
@@ -435,31 +434,51 @@ __device__ bool finish_pick(const FusedArgs& a, FuShared& sh, int b, int ctid, u
       double v = static_cast<double>(acc);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) sh.wsum[warp] = v;
-      if (!group_sync(sh, gphase, a.timeout_ns)) return false;
-      if (ctid == 0) {
-        double t = 0.0;
-        for (int w = 0; w < FU_CW; ++w) t += sh.wsum[w];
-        sh.sl[j] = t;
-      }
-      if (!group_sync(sh, gphase, a.timeout_ns)) return false;
+      if ((j & 31) == lane) sl[j >> 5] = v;
     }
   }
-  const int js = sh.jstar;
+  const double target = static_cast<double>(inf.u1) * R;
+  // slice holding the target: inclusive prefix over slices (lane order, then +32)
+  double pre0 = sl[0];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, pre0, o);
+    if (lane >= o) pre0 += y;
+  }
+  const double tot0 = __shfl_sync(0xffffffffu, pre0, 31);
+  double pre1 = sl[1];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, pre1, o);
+    if (lane >= o) pre1 += y;
+  }
+  pre1 += tot0;
+  const unsigned hit0 = __ballot_sync(0xffffffffu, sl[0] > 0.0 && pre0 > target);
+  const unsigned hit1 = __ballot_sync(0xffffffffu, sl[1] > 0.0 && pre1 > target);
+  const unsigned pos0 = __ballot_sync(0xffffffffu, sl[0] > 0.0);
+  const unsigned pos1 = __ballot_sync(0xffffffffu, sl[1] > 0.0);
+  int js;
+  if (hit0) js = __ffs(hit0) - 1;
+  else if (hit1) js = 32 + __ffs(hit1) - 1;
+  else if (pos1) js = 32 + 31 - __clz(pos1);   // rounding: the last slice with mass
+  else if (pos0) js = 31 - __clz(pos0);
+  else js = -1;
   int pick = -1;
   if (js >= 0) {
+    const double ex0 = __shfl_sync(0xffffffffu, pre0 - sl[0], js & 31);
+    const double ex1 = __shfl_sync(0xffffffffu, pre1 - sl[1], js & 31);
+    const double base = js < 32 ? ex0 : ex1;
     const int e0 = js * a.Lr;
     const int n = min(V, e0 + a.Lr) - e0;
-    int seg = (n + FU_CT - 1) / FU_CT;
+    int seg = (n + 31) / 32;
     seg = (seg + 7) / 8 * 8;
-    const int k0 = min(n, ctid * seg), k1 = min(n, k0 + seg);
+    const int k0 = min(n, lane * seg), k1 = min(n, k0 + seg);
     float Tt = 0.f;
     int lastpos = -1;
     for (int k = k0; k < k1; k += 8) {
       float zp[8], zq[8];
       load8_global<TP>(prow + static_cast<long long>(e0 + k) * TP::esz, zp);
-      if (has_q) load8_global<typename std::conditional<QE == 4, F32T, BF16T>::type>(
-          qrow + static_cast<long long>(e0 + k) * QE, zq);
+      if (has_q) load8_global<QT>(qrow + static_cast<long long>(e0 + k) * QT::esz, zq);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float w = resid_w(zp[i], has_q ? zq[i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q, PROBS);
@@ -473,56 +492,44 @@ __device__ bool finish_pick(const FusedArgs& a, FuShared& sh, int b, int ctid, u
       const double y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
-    if (lane == 31) sh.wsum[warp] = x;
-    int lp = lastpos;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
-    if (lane == 0 && lp >= 0) atomicMax(&sh.lastpos, lp);
-    if (!group_sync(sh, gphase, a.timeout_ns)) return false;
-    double wex = 0.0;
-    for (int w = 0; w < warp; ++w) wex += sh.wsum[w];
-    const double base = sh.base + wex + (x - static_cast<double>(Tt));
-    const double target = sh.target;
-    if (Tt > 0.f && base <= target && base + static_cast<double>(Tt) > target) {
+    const double lb = base + (x - static_cast<double>(Tt));
+    const bool owner = Tt > 0.f && lb <= target && lb + static_cast<double>(Tt) > target;
+    int cand = 0x7fffffff;
+    if (owner) {
       float run = 0.f;
-      for (int k = k0; k < k1; k += 8) {
+      for (int k = k0; k < k1 && cand == 0x7fffffff; k += 8) {
         float zp[8], zq[8];
         load8_global<TP>(prow + static_cast<long long>(e0 + k) * TP::esz, zp);
-        if (has_q) load8_global<typename std::conditional<QE == 4, F32T, BF16T>::type>(
-            qrow + static_cast<long long>(e0 + k) * QE, zq);
-        int found = -1;
+        if (has_q) load8_global<QT>(qrow + static_cast<long long>(e0 + k) * QT::esz, zq);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float w = resid_w(zp[i], has_q ? zq[i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q, PROBS);
           run += w;
-          if (found < 0 && base + static_cast<double>(run) > target) found = i;
-        }
-        if (found >= 0) {
-          atomicMin(&sh.pick, e0 + k + found);
-          break;
+          if (cand == 0x7fffffff && lb + static_cast<double>(run) > target) cand = e0 + k + i;
         }
       }
     }
-    if (!group_sync(sh, gphase, a.timeout_ns)) return false;
-    pick = (sh.pick != 0x7fffffff) ? sh.pick : sh.lastpos;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+      lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, o));
+    }
+    pick = cand != 0x7fffffff ? cand : lastpos;
   }
-  if (ctid == 0) a.out_tokens[static_cast<long long>(b) * W + inf.tstar] = pick;
-  if (b == a.debug_b && sh.R > 0.0) {
-    const double R = sh.R;
-    for (int g = ctid; g < V / 8; g += FU_CT) {
+  if (lane == 0) a.out_tokens[static_cast<long long>(b) * W + inf.tstar] = pick;
+  if (b == a.debug_b && R > 0.0) {
+    for (int g = lane; g < V / 8; g += 32) {
       float zp[8], zq[8];
       load8_global<TP>(prow + static_cast<long long>(g) * 8 * TP::esz, zp);
-      if (has_q) load8_global<typename std::conditional<QE == 4, F32T, BF16T>::type>(
-          qrow + static_cast<long long>(g) * 8 * QE, zq);
+      if (has_q) load8_global<QT>(qrow + static_cast<long long>(g) * 8 * QT::esz, zq);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float w = resid_w(zp[i], has_q ? zq[i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q, PROBS);
         a.debug_row[g * 8 + i] = static_cast<float>(static_cast<double>(w) / R);
       }
     }
-    if (ctid == 0) *a.debug_mass = static_cast<float>(R);
+    if (lane == 0) *a.debug_mass = static_cast<float>(R);
   }
-  return group_sync(sh, gphase, a.timeout_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -530,7 +537,7 @@ __device__ bool finish_pick(const FusedArgs& a, FuShared& sh, int b, int ctid, u
 // ---------------------------------------------------------------------------
 template <class TP, class TQ, bool PROBS>
 __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& sh) {
-  constexpr int QE = PROBS ? 4 : TQ::esz;
+  using QT = typename std::conditional<PROBS, F32T, TQ>::type;
   int stage = 0;
   uint32_t phase = 0;
   int last_parity[FU_NSTAGE];
@@ -539,13 +546,12 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
   const unsigned RU = static_cast<unsigned>(a.B) * static_cast<unsigned>(a.Sr);
   const unsigned per_seq = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S);
   const int W = a.K + 1;
-  bool sweep_done = false;
+  unsigned next_sweep = blockIdx.x;
 
   auto next_stage = [&]() -> bool {
     if (fu_aborted(sh)) return false;
     if (!mbar_wait(&sh.empty[stage], phase ^ 1u, a.timeout_ns)) {
-      fu_set_abort(sh);
-      atomicOr(&a.ctl->err, 1u);
+      fu_fail(sh, a.ctl, 1u);
       return false;
     }
     return true;
@@ -556,28 +562,28 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
 
   bool ok = true;
   while (ok) {
-    // 1. a queued residual unit, if one is ready
+    // a published residual unit first (claimed through one packed word)
     long long rid = -1;
-    unsigned rn = *reinterpret_cast<volatile unsigned*>(&a.ctl->rnext);
-    unsigned rr = *reinterpret_cast<volatile unsigned*>(&a.ctl->rres);
-    for (int tries = 0; tries < 8 && rn < rr; ++tries) {
-      const unsigned prev = atomicCAS(&a.ctl->rnext, rn, rn + 1);
-      if (prev == rn) { rid = rn; break; }
-      rn = prev;
-      rr = *reinterpret_cast<volatile unsigned*>(&a.ctl->rres);
+    {
+      unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(&a.ctl->rq);
+      for (int tries = 0; tries < 4 && static_cast<unsigned>(v >> 32) < static_cast<unsigned>(v); ++tries) {
+        const unsigned long long prev = atomicCAS(&a.ctl->rq, v, v + (1ull << 32));
+        if (prev == v) { rid = static_cast<long long>(v >> 32); break; }
+        v = prev;
+      }
     }
-    // 2. otherwise a sweep unit
     long long uid = -1;
-    if (rid < 0 && !sweep_done) {
-      const unsigned u = atomicAdd(&a.ctl->next, 1u);
-      if (u < a.U) uid = u;
-      else sweep_done = true;
-    }
-    // 3. sweep exhausted: the next residual unit, waiting for it if needed
-    if (rid < 0 && uid < 0) {
-      const unsigned r = atomicAdd(&a.ctl->rnext, 1u);
-      if (r >= RU) break;
-      rid = r;
+    if (rid < 0) {
+      if (next_sweep < a.U) {
+        uid = next_sweep;
+        next_sweep += gridDim.x;
+      } else {
+        // sweep done: the next residual unit, waiting for its publication
+        const unsigned long long v = atomicAdd(&a.ctl->rq, 1ull << 32);
+        const unsigned r = static_cast<unsigned>(v >> 32);
+        if (r >= RU) break;
+        rid = r;
+      }
     }
     if (uid >= 0) {
       const unsigned u = static_cast<unsigned>(uid);
@@ -586,7 +592,7 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
       const int row = static_cast<int>(rem / a.S);
       const int j = static_cast<int>(rem - static_cast<unsigned>(row) * a.S);
       const bool is_draft = row >= W;
-      const int esz = is_draft ? QE : TP::esz;
+      const int esz = is_draft ? QT::esz : TP::esz;
       const unsigned char* src =
           is_draft ? a.draft + ((static_cast<long long>(b) * a.K + (row - W)) * a.V) * esz
                    : a.target + ((static_cast<long long>(b) * W + row) * a.V) * esz;
@@ -603,23 +609,22 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
         d.n = static_cast<int>(n);   // bytes for sweep stages
         d.flags = (off == 0 ? FL_FIRST : 0) | (off + n >= bytes ? FL_LAST : 0) | (is_draft ? FL_DRAFT : 0);
         mbar_arrive_expect_tx(&sh.full[stage], n);
-        bulk_g2s(ring + stage * FU_STAGE, src + e0 * esz + off, n, &sh.full[stage]);
+        bulk_g2s(ring + stage * FU_STAGE, src + static_cast<long long>(e0) * esz + off, n, &sh.full[stage]);
         last_parity[stage] = static_cast<int>(phase);
         advance();
       }
       continue;
     }
-    // residual unit rid: wait for its queue entry (written by a finished scan)
+    // residual unit rid: its queue entry is written by the scan that reserved it
     unsigned ent = ld_acquire_u32(a.queue + rid);
     if (ent == 0) {
       const uint64_t t0 = global_ns();
       while ((ent = ld_acquire_u32(a.queue + rid)) == 0) {
         if (fu_aborted(sh) || global_ns() - t0 > a.timeout_ns) break;
-        __nanosleep(256);
+        __nanosleep(200);
       }
       if (ent == 0) {
-        fu_set_abort(sh);
-        atomicOr(&a.ctl->err, 2u);
+        fu_fail(sh, a.ctl, 2u);
         break;
       }
     }
@@ -633,6 +638,7 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
       for (int i = 0; i < 8; ++i) dst[i] = __ldcg(src + i);
     }
     if (inf.status != 0) {
+      // invalid sequence: a data-less stage, so the arrivals are still counted
       if (!next_stage()) break;
       StageDesc& d = sh.desc[stage];
       d.kind = KIND_RESID;
@@ -641,16 +647,15 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
       d.e0 = 0;
       d.n = 0;
       d.flags = FL_FIRST | FL_LAST;
-      d.status = inf.status;
       mbar_arrive(&sh.full[stage]);
-      // the stage was released, so its previous copy has landed: nothing to drain
-      last_parity[stage] = -1;
+      last_parity[stage] = -1;   // the stage was released: its previous copy has landed
       advance();
       continue;
     }
     const bool has_q = inf.tstar < a.K;
     const unsigned char* prow = a.target + ((static_cast<long long>(b) * W + inf.tstar) * a.V) * TP::esz;
-    const unsigned char* qrow = has_q ? a.draft + ((static_cast<long long>(b) * a.K + inf.tstar) * a.V) * QE : nullptr;
+    const unsigned char* qrow =
+        has_q ? a.draft + ((static_cast<long long>(b) * a.K + inf.tstar) * a.V) * QT::esz : nullptr;
     const int e0 = j * a.Lr, e1 = min(a.V, e0 + a.Lr);
     for (int e = e0; e < e1; e += a.RE) {
       const int n = min(a.RE, e1 - e);
@@ -662,17 +667,16 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
       d.e0 = e;
       d.n = n;   // elements for residual stages
       d.flags = (e == e0 ? FL_FIRST : 0) | (e + n >= e1 ? FL_LAST : 0) | (has_q ? FL_HASQ : 0);
-      d.status = 0;
       d.tstar = inf.tstar;
       d.AP = inf.AP;
       d.AQ = inf.AQ;
       d.iSp = inf.iSp;
       d.iSq = inf.iSq;
-      const uint32_t bp = static_cast<uint32_t>(n * TP::esz), bq = has_q ? static_cast<uint32_t>(n * QE) : 0u;
+      const uint32_t bp = static_cast<uint32_t>(n * TP::esz), bq = has_q ? static_cast<uint32_t>(n * QT::esz) : 0u;
       mbar_arrive_expect_tx(&sh.full[stage], bp + bq);
       unsigned char* dst = ring + stage * FU_STAGE;
       bulk_g2s(dst, prow + static_cast<long long>(e) * TP::esz, bp, &sh.full[stage]);
-      if (has_q) bulk_g2s(dst + a.RE * TP::esz, qrow + static_cast<long long>(e) * QE, bq, &sh.full[stage]);
+      if (has_q) bulk_g2s(dst + a.RE * TP::esz, qrow + static_cast<long long>(e) * QT::esz, bq, &sh.full[stage]);
       last_parity[stage] = static_cast<int>(phase);
       advance();
     }
@@ -686,11 +690,129 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
   // Do not leave while a copy may still land in this CTA's shared memory.  A
   // stage's recorded parity is that of its last copy; any later arrival on the
   // stage (which would flip the phase again) clears the record, so a wait here
-  // can only be for a copy that has not been consumed yet (abort path).
+  // is only for a copy that has not been consumed (abort path).
 #pragma unroll
   for (int s = 0; s < FU_NSTAGE; ++s)
     if (last_parity[s] >= 0 && !mbar_wait(&sh.full[s], static_cast<uint32_t>(last_parity[s]), a.timeout_ns))
       atomicOr(&a.ctl->err, 8u);
+}
+
+// ---------------------------------------------------------------------------
+// consumers (eight warps)
+// ---------------------------------------------------------------------------
+template <class TP, class TQ, bool PROBS>
+__device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& sh, int cw, int lane) {
+  const int ctid = cw * 32 + lane;
+  const unsigned per_seq = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S) * FU_CW;
+  const unsigned per_res = static_cast<unsigned>(a.Sr) * FU_CW;
+  int stage = 0;
+  uint32_t phase = 0;
+  StatsAcc sacc;
+  sacc.init();
+  float racc = 0.f;
+  for (;;) {
+    if (__any_sync(0xffffffffu, fu_aborted(sh))) break;
+    if (!__all_sync(0xffffffffu, mbar_wait(&sh.full[stage], phase, a.timeout_ns))) {
+      fu_fail(sh, a.ctl, 4u);
+      break;
+    }
+    const StageDesc d = sh.desc[stage];
+    if (d.kind == KIND_STOP) break;
+    if (d.flags & FL_FIRST) {
+      sacc.init();
+      racc = 0.f;
+    }
+    const unsigned char* buf = ring + stage * FU_STAGE;
+    if (d.kind == KIND_SWEEP) {
+      if (d.flags & FL_DRAFT) {
+        if constexpr (!PROBS) stats_stage<TQ>(reinterpret_cast<const uint4*>(buf), d.n >> 4, ctid, a.c, sacc);
+      } else {
+        stats_stage<TP>(reinterpret_cast<const uint4*>(buf), d.n >> 4, ctid, a.c, sacc);
+      }
+    } else if (d.n > 0) {
+      racc += resid_stage<TP, TQ, PROBS>(buf, d, a.RE, ctid, a.c);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[stage]);
+    if (++stage == FU_NSTAGE) { stage = 0; phase ^= 1u; }
+    if (!(d.flags & FL_LAST)) continue;
+
+    // end of a work item: this warp's partial, counted in the sequence's arrivals
+    int task = 0;
+    if (d.kind == KIND_SWEEP) {
+      sacc.warp_reduce(a.c);
+      if (lane == 0) {
+        a.part[static_cast<long long>(d.unit) * FU_CW + cw] = sacc.pack();
+        __threadfence();
+        const unsigned old = atomicAdd(&a.cnt1[d.b], 1u);
+        if (old + 1u == per_seq) task = (d.b << 1 | 0) + 1;
+      }
+    } else {
+      double v = static_cast<double>(racc);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) {
+        a.rpart[(static_cast<long long>(d.b) * a.Sr + d.unit) * FU_CW + cw] = v;
+        __threadfence();
+        const unsigned old = atomicAdd(&a.cnt2[d.b], 1u);
+        if (old + 1u == per_res) task = (d.b << 1 | 1) + 1;
+      }
+    }
+    if (lane == 0 && task) {
+      __threadfence();
+      // hand the finished sequence to the finisher warp (bounded wait for space)
+      const unsigned slot = atomicAdd(&sh.task_tail, 1u);
+      volatile int* q = reinterpret_cast<volatile int*>(&sh.task[slot % FU_TASKQ]);
+      const uint64_t t0 = global_ns();
+      while (*q != 0) {
+        if (global_ns() - t0 > a.timeout_ns) { fu_fail(sh, a.ctl, 16u); break; }
+        __nanosleep(100);
+      }
+      *q = task;
+    }
+    __syncwarp();
+  }
+  __syncwarp();
+  if (lane == 0) atomicAdd(&sh.cons_done, 1);
+}
+
+// ---------------------------------------------------------------------------
+// finisher (one warp): takes tasks from the CTA's queue until the consumers
+// have left and the queue is empty
+// ---------------------------------------------------------------------------
+template <class TP, class TQ, bool PROBS>
+__device__ void fu_finisher(const FusedArgs& a, FuShared& sh, int lane) {
+  unsigned head = 0;
+  uint64_t idle_since = global_ns();
+  for (;;) {
+    int task = 0;
+    if (lane == 0) task = *reinterpret_cast<volatile int*>(&sh.task[head % FU_TASKQ]);
+    task = __shfl_sync(0xffffffffu, task, 0);
+    if (task != 0) {
+      if (lane == 0) *reinterpret_cast<volatile int*>(&sh.task[head % FU_TASKQ]) = 0;
+      ++head;
+      __threadfence();
+      const int b = (task - 1) >> 1;
+      if (((task - 1) & 1) == 0) finish_scan<TP, TQ, PROBS>(a, b, lane);
+      else finish_pick<TP, TQ, PROBS>(a, b, lane);
+      __syncwarp();
+      idle_since = global_ns();
+      continue;
+    }
+    int done = 0;
+    if (lane == 0) {
+      const int cd = *reinterpret_cast<volatile int*>(&sh.cons_done);
+      const unsigned tail = *reinterpret_cast<volatile unsigned*>(&sh.task_tail);
+      done = (cd == FU_CW && tail == head) || fu_aborted(sh);
+    }
+    if (__shfl_sync(0xffffffffu, done, 0)) break;
+    // bounded: the consumers' own waits end (and they leave) well before this
+    if (global_ns() - idle_since > 4 * a.timeout_ns) {
+      if (lane == 0) fu_fail(sh, a.ctl, 32u);
+      break;
+    }
+    __nanosleep(128);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -709,93 +831,20 @@ __global__ void __launch_bounds__(FU_THREADS, 3) fused_sample_kernel(const Fused
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], FU_CW);
     }
-    mbar_init(&sh.gbar, FU_CW);
+    for (int i = 0; i < FU_TASKQ; ++i) sh.task[i] = 0;
+    sh.task_tail = 0;
+    sh.cons_done = 0;
     sh.abort = 0;
-    sh.pick = 0x7fffffff;
-    sh.lastpos = -1;
     mbar_fence_init();
   }
   __syncthreads();
 
   if (warp == 0) {
     if (lane == 0) fu_producer<TP, TQ, PROBS>(a, ring, sh);
+  } else if (warp == FU_FIN_WARP) {
+    fu_finisher<TP, TQ, PROBS>(a, sh, lane);
   } else {
-    const int ctid = threadIdx.x - 32, cw = warp - 1;
-    int stage = 0;
-    uint32_t phase = 0, gphase = 0;
-    StatsAcc sacc;
-    sacc.init();
-    float racc = 0.f;
-    const unsigned per_seq = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S);
-    for (;;) {
-      if (__any_sync(0xffffffffu, fu_aborted(sh))) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sh.full[stage], phase, a.timeout_ns))) {
-        fu_set_abort(sh);
-        atomicOr(&a.ctl->err, 4u);
-        break;
-      }
-      const StageDesc d = sh.desc[stage];
-      if (d.kind == KIND_STOP) break;
-      if (d.flags & FL_FIRST) {
-        sacc.init();
-        racc = 0.f;
-      }
-      const unsigned char* buf = ring + stage * FU_STAGE;
-      if (d.kind == KIND_SWEEP) {
-        if (d.flags & FL_DRAFT) {
-          if constexpr (!PROBS) stats_stage<TQ>(reinterpret_cast<const uint4*>(buf), d.n >> 4, ctid, a.c, sacc);
-        } else {
-          stats_stage<TP>(reinterpret_cast<const uint4*>(buf), d.n >> 4, ctid, a.c, sacc);
-        }
-      } else if (d.n > 0) {
-        racc += resid_stage<TP, TQ, PROBS>(buf, d, a.RE, ctid, a.c);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.empty[stage]);
-      if (++stage == FU_NSTAGE) { stage = 0; phase ^= 1u; }
-      if (!(d.flags & FL_LAST)) continue;
-
-      // ---- end of a work unit: reduce across the consumer warps ----------
-      if (d.kind == KIND_SWEEP) {
-        sacc.warp_reduce(a.c);
-        if (lane == 0) sh.red2[cw] = sacc.pack();
-      } else {
-        double v = static_cast<double>(racc);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) sh.redd[cw] = v;
-      }
-      if (!group_sync(sh, gphase, a.timeout_ns)) break;
-      if (cw == 0) {
-        if (d.kind == KIND_SWEEP) {
-          StatsAcc t;
-          t.init();
-          if (lane < FU_CW) t.unpack(sh.red2[lane]);
-          t.warp_reduce(a.c);
-          if (lane == 0) {
-            a.part[d.unit] = t.pack();
-            __threadfence();
-            const unsigned old = atomicAdd(&a.cnt1[d.b], 1u);
-            sh.flag_last = (old + 1u == per_seq);
-            if (sh.flag_last) __threadfence();
-          }
-        } else if (lane == 0) {
-          double tot = 0.0;
-          for (int w = 0; w < FU_CW; ++w) tot += sh.redd[w];
-          a.rsum[static_cast<long long>(d.b) * a.Sr + d.unit] = d.n > 0 ? tot : 0.0;
-          __threadfence();
-          const unsigned old = atomicAdd(&a.cnt2[d.b], 1u);
-          sh.flag_last = (old + 1u == static_cast<unsigned>(a.Sr));
-          if (sh.flag_last) __threadfence();
-        }
-      }
-      if (!group_sync(sh, gphase, a.timeout_ns)) break;
-      if (__shfl_sync(0xffffffffu, sh.flag_last, 0)) {
-        const bool ok = d.kind == KIND_SWEEP ? finish_scan<TP, TQ, PROBS>(a, sh, d.b, ctid, gphase)
-                                             : finish_pick<TP, TQ, PROBS>(a, sh, d.b, ctid, gphase);
-        if (!ok) break;
-      }
-    }
+    fu_consumer<TP, TQ, PROBS>(a, ring, sh, warp - 1, lane);
   }
   __syncwarp();
   __syncthreads();

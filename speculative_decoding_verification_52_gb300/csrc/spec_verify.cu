@@ -48,8 +48,8 @@ constexpr int kMaxDevices = 64;
 constexpr unsigned long long kWaitNs = 1000000000ull;   // bounded waits: 1 s
 
 int max_slices(int V) { return std::max(1, (V + kMinSlice - 1) / kMinSlice); }
-// residual slices of the fused sampling kernel are >= 8192 elements
-int max_rslices(int V) { return std::max(1, (V + 8191) / 8192); }
+// residual slices of the fused sampling kernel: >= 4096 elements, at most 64 per row
+int max_rslices(int V) { return std::min(64, std::max(1, (V + 4095) / 4096)); }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -284,20 +284,20 @@ int finish_max_cluster(int dev) {
 }
 
 // Workspace of the fused sampling kernel:
-//   [FuCtl | cnt1[B] | cnt2[B] | queue[B*Sr]]  zeroed per call
-//   [info[B] | rsum[B*Sr] | part[rows*S]]
+//   [FuCtl | cnt1[B] | cnt2[B] | queue[B*Sr]]        zeroed per call
+//   [info[B] | rpart[B*Sr*8] (double) | part[rows*S*8] (float2)]
 struct FusedLayout {
-  size_t zero_bytes, info_off, rsum_off, part_off, total;
+  size_t zero_bytes, info_off, rpart_off, part_off, total;
 };
 FusedLayout fused_layout(int B, int K, int V) {
   FusedLayout l{};
   const size_t sr = static_cast<size_t>(max_rslices(V));
-  l.zero_bytes = align_up(sizeof(FuCtl) + 8u * static_cast<size_t>(B) + 4u * static_cast<size_t>(B) * sr, 16);
+  l.zero_bytes = align_up(32 + 8u * static_cast<size_t>(B) + 4u * static_cast<size_t>(B) * sr, 16);
   l.info_off = l.zero_bytes;
-  l.rsum_off = align_up(l.info_off + sizeof(SeqInfo) * static_cast<size_t>(B), 16);
-  l.part_off = align_up(l.rsum_off + sizeof(double) * static_cast<size_t>(B) * sr, 16);
+  l.rpart_off = align_up(l.info_off + sizeof(SeqInfo) * static_cast<size_t>(B), 16);
+  l.part_off = align_up(l.rpart_off + sizeof(double) * FU_CW * static_cast<size_t>(B) * sr, 16);
   const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(2 * K + 1);
-  l.total = align_up(l.part_off + rows * static_cast<size_t>(max_slices(V)) * sizeof(float2), 256);
+  l.total = align_up(l.part_off + rows * static_cast<size_t>(max_slices(V)) * FU_CW * sizeof(float2), 256);
   return l;
 }
 
@@ -340,9 +340,10 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   const long long U = rows * S;
   if (U >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "batch too large for one call");
   const int RE = (TP::esz == 2 && QE == 2) ? 4096 : 2048;
-  const int Lr = 4 * RE;
+  int Lr = 2 * RE;
+  if (ceil_div(V, Lr) > FU_MAX_SR) Lr = ceil_div(ceil_div(V, FU_MAX_SR), RE) * RE;
   const int Sr = ceil_div(V, Lr);
-  if (Sr > FU_MAX_SR || Sr > max_rslices(V)) return fail(SPEC_ERR_UNSUPPORTED, "V=%d too large", V);
+  if (Sr > max_rslices(V)) return fail(SPEC_ERR_UNSUPPORTED, "V=%d too large", V);
 
   const FusedLayout lay = fused_layout(B, K, V);
   unsigned char* w = static_cast<unsigned char*>(ws);
@@ -363,11 +364,11 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   a.U = static_cast<unsigned>(U);
   a.c = c;
   a.ctl = reinterpret_cast<FuCtl*>(w);
-  a.cnt1 = reinterpret_cast<unsigned*>(w + sizeof(FuCtl));
+  a.cnt1 = reinterpret_cast<unsigned*>(w + 32);
   a.cnt2 = a.cnt1 + B;
   a.queue = a.cnt2 + B;
   a.info = reinterpret_cast<SeqInfo*>(w + lay.info_off);
-  a.rsum = reinterpret_cast<double*>(w + lay.rsum_off);
+  a.rpart = reinterpret_cast<double*>(w + lay.rpart_off);
   a.part = reinterpret_cast<float2*>(w + lay.part_off);
   a.out_tokens = out;
   a.num_accepted = nacc;
