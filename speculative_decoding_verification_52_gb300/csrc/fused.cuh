@@ -100,6 +100,7 @@ struct FuShared {
   uint64_t full[FU_NSTAGE];
   uint64_t empty[FU_NSTAGE];
   StageDesc desc[FU_NSTAGE];
+  int unit_cnt[FU_NSTAGE];       // consumer warps done with the work item ending in this stage
   int task[FU_TASKQ];            // (b << 1 | kind) + 1, 0 = empty slot
   unsigned task_tail;            // next slot to fill (shared-memory atomics)
   int cons_done;                 // consumer warps that have left
@@ -267,35 +268,64 @@ template <class TP, class TQ, bool PROBS>
 __device__ void finish_scan(const FusedArgs& a, int b, int lane) {
   const int K = a.K, W = K + 1, V = a.V;
   const int npart = a.S * FU_CW;
-  // lane owns rows lane and lane + 32: merge their S x 8 warp partials
+  // merge each row's S x 8 warp partials with the whole warp (rows in groups
+  // of 8, all loads of a group in flight together); row r ends up in lane
+  // r & 31, register r >> 5
   float Ar[2] = {0.f, 0.f};
   double Sr[2] = {0.0, 0.0};
   int st[2] = {1, 1};
+  for (int r0 = 0; r0 < a.RB; r0 += 8) {
+    float2 pv[8][2];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = lane + 32 * h;
-    if (r >= a.RB) continue;
-    const float2* part = a.part + (static_cast<long long>(b) * a.RB + r) * npart;
-    float M = kNegInf;
-    bool poison = false;
-    for (int i = 0; i < npart; ++i) {
-      const float2 p = __ldcg(part + i);
-      if (p.x != p.x) poison = true;
-      else M = fmaxf(M, p.x);
+    for (int g = 0; g < 8; ++g)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = r0 + g, i = lane + 32 * h;
+        pv[g][h] = (r < a.RB && i < npart) ? __ldcg(a.part + (static_cast<long long>(b) * a.RB + r) * npart + i)
+                                            : make_float2(kNegInf, 0.f);
+      }
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const int r = r0 + g;
+      if (r >= a.RB) break;
+      // partials beyond 64 per row (small batches with many slices)
+      float M = kNegInf;
+      bool poison = false;
+      for (int i = 64 + lane; i < npart; i += 32) {
+        const float2 p = __ldcg(a.part + (static_cast<long long>(b) * a.RB + r) * npart + i);
+        if (p.x != p.x) poison = true;
+        else M = fmaxf(M, p.x);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (pv[g][h].x != pv[g][h].x) poison = true;
+        else M = fmaxf(M, pv[g][h].x);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      poison = __any_sync(0xffffffffu, poison);
+      const float AM = (M == kNegInf || poison) ? 0.f : __fmul_rn(M, a.c);
+      double acc = 0.0;
+      if (!poison && M != kNegInf) {
+        // fl(m*c) - fl(M*c) is exact in fp32 whenever the factor is not negligible
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (pv[g][h].x != kNegInf)
+            acc += static_cast<double>(pv[g][h].y) * static_cast<double>(exp2f(__fmul_rn(pv[g][h].x, a.c) - AM));
+        for (int i = 64 + lane; i < npart; i += 32) {
+          const float2 p = __ldcg(a.part + (static_cast<long long>(b) * a.RB + r) * npart + i);
+          if (p.x != kNegInf) acc += static_cast<double>(p.y) * static_cast<double>(exp2f(__fmul_rn(p.x, a.c) - AM));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      }
+      const int state = poison ? 2 : (M == kNegInf ? 1 : ((isfinite(acc) && acc > 0.0) ? 0 : 1));
+      if (lane == (r & 31)) {
+        Ar[r >> 5] = AM;
+        Sr[r >> 5] = acc;
+        st[r >> 5] = state;
+      }
     }
-    if (poison) { st[h] = 2; continue; }
-    if (M == kNegInf) { st[h] = 1; continue; }
-    const float AM = __fmul_rn(M, a.c);
-    double acc = 0.0;
-    for (int i = 0; i < npart; ++i) {
-      const float2 p = __ldcg(part + i);
-      if (p.x == kNegInf) continue;
-      // fl(m*c) - fl(M*c) is exact in fp32 whenever the factor is not negligible
-      acc += static_cast<double>(p.y) * static_cast<double>(exp2f(__fmul_rn(p.x, a.c) - AM));
-    }
-    Ar[h] = AM;
-    Sr[h] = acc;
-    st[h] = (isfinite(acc) && acc > 0.0) ? 0 : 1;
   }
 
   // lane t tests position t
@@ -703,8 +733,8 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
 template <class TP, class TQ, bool PROBS>
 __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& sh, int cw, int lane) {
   const int ctid = cw * 32 + lane;
-  const unsigned per_seq = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S) * FU_CW;
-  const unsigned per_res = static_cast<unsigned>(a.Sr) * FU_CW;
+  const unsigned per_seq = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S);
+  const unsigned per_res = static_cast<unsigned>(a.Sr);
   int stage = 0;
   uint32_t phase = 0;
   StatsAcc sacc;
@@ -722,6 +752,7 @@ __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& s
       sacc.init();
       racc = 0.f;
     }
+    const int cur = stage;
     const unsigned char* buf = ring + stage * FU_STAGE;
     if (d.kind == KIND_SWEEP) {
       if (d.flags & FL_DRAFT) {
@@ -732,31 +763,40 @@ __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& s
     } else if (d.n > 0) {
       racc += resid_stage<TP, TQ, PROBS>(buf, d, a.RE, ctid, a.c);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.empty[stage]);
     if (++stage == FU_NSTAGE) { stage = 0; phase ^= 1u; }
-    if (!(d.flags & FL_LAST)) continue;
+    if (!(d.flags & FL_LAST)) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[cur]);
+      continue;
+    }
 
-    // end of a work item: this warp's partial, counted in the sequence's arrivals
+    // End of a work item: this warp writes its partial; the CTA counts its
+    // warps in shared memory, and the last one counts the item in the
+    // sequence's global arrival counter (one global atomic per item).
     int task = 0;
     if (d.kind == KIND_SWEEP) {
       sacc.warp_reduce(a.c);
-      if (lane == 0) {
-        a.part[static_cast<long long>(d.unit) * FU_CW + cw] = sacc.pack();
-        __threadfence();
-        const unsigned old = atomicAdd(&a.cnt1[d.b], 1u);
-        if (old + 1u == per_seq) task = (d.b << 1 | 0) + 1;
-      }
     } else {
-      double v = static_cast<double>(racc);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) {
-        a.rpart[(static_cast<long long>(d.b) * a.Sr + d.unit) * FU_CW + cw] = v;
+      for (int o = 16; o > 0; o >>= 1) racc += __shfl_xor_sync(0xffffffffu, racc, o);
+    }
+    if (lane == 0) {
+      if (d.kind == KIND_SWEEP) a.part[static_cast<long long>(d.unit) * FU_CW + cw] = sacc.pack();
+      else a.rpart[(static_cast<long long>(d.b) * a.Sr + d.unit) * FU_CW + cw] = static_cast<double>(racc);
+      __threadfence_block();
+      const int prev = atomicAdd(&sh.unit_cnt[cur], 1);
+      if (prev == FU_CW - 1) {
+        sh.unit_cnt[cur] = 0;   // the slot's next item starts only after this warp releases it
         __threadfence();
-        const unsigned old = atomicAdd(&a.cnt2[d.b], 1u);
-        if (old + 1u == per_res) task = (d.b << 1 | 1) + 1;
+        if (d.kind == KIND_SWEEP) {
+          const unsigned old = atomicAdd(&a.cnt1[d.b], 1u);
+          if (old + 1u == per_seq) task = (d.b << 1 | 0) + 1;
+        } else {
+          const unsigned old = atomicAdd(&a.cnt2[d.b], 1u);
+          if (old + 1u == per_res) task = (d.b << 1 | 1) + 1;
+        }
       }
+      mbar_arrive(&sh.empty[cur]);
     }
     if (lane == 0 && task) {
       __threadfence();
@@ -832,6 +872,7 @@ __global__ void __launch_bounds__(FU_THREADS, 3) fused_sample_kernel(const Fused
       mbar_init(&sh.empty[s], FU_CW);
     }
     for (int i = 0; i < FU_TASKQ; ++i) sh.task[i] = 0;
+    for (int i = 0; i < FU_NSTAGE; ++i) sh.unit_cnt[i] = 0;
     sh.task_tail = 0;
     sh.cons_done = 0;
     sh.abort = 0;

@@ -332,11 +332,24 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   // sweep slices: ~48 KB units, but at least two units per CTA when the batch is small
   const int smax = max_slices(V);
   const long long row_bytes = static_cast<long long>(V) * std::max(TP::esz, QE);
-  int S = std::max(1, ceil_div(row_bytes, 49152));
-  S = std::max(S, static_cast<int>(std::min<long long>(smax, (2LL * grid_cap + rows - 1) / rows)));
-  S = std::min(S, smax);
-  int L = (ceil_div(V, S) + 7) / 8 * 8;
+  int S0 = std::max(1, ceil_div(row_bytes, 49152));
+  S0 = std::max(S0, static_cast<int>(std::min<long long>(smax, (2LL * grid_cap + rows - 1) / rows)));
+  S0 = std::min(S0, smax);
+  // Units are dealt round-robin and numbered sequence-major, so the last unit of
+  // sequence b lands on CTA (RB*S*(b+1) - 1) mod grid.  Choose S (or trim the
+  // grid) so that RB*S and the grid are coprime: completions -- and the scan
+  // tasks they create -- then rotate through all CTAs instead of a few.
+  auto gcd = [](long long x, long long y) { while (y) { const long long t = x % y; x = y; y = t; } return x; };
+  int S = S0, L = (ceil_div(V, S0) + 7) / 8 * 8, grid = grid_cap;
   S = ceil_div(V, L);
+  bool found = false;
+  for (int s_try = S0; s_try <= std::min(smax, S0 + 8) && !found; ++s_try) {
+    const int l = (ceil_div(V, s_try) + 7) / 8 * 8;
+    const int se = ceil_div(V, l);
+    if (gcd(static_cast<long long>(RB) * se, grid_cap) == 1) { S = se; L = l; found = true; }
+  }
+  for (int g = grid_cap; g > grid_cap - 32 && g > 1 && !found; --g)
+    if (gcd(static_cast<long long>(RB) * S, g) == 1) { grid = g; found = true; }
   const long long U = rows * S;
   if (U >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "batch too large for one call");
   const int RE = (TP::esz == 2 && QE == 2) ? 4096 : 2048;
@@ -381,7 +394,7 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   if (e != cudaSuccess) return cuda_fail(e, "workspace control reset");
   prof_mark(0, st);
   const long long work = U + static_cast<long long>(B) * Sr;
-  const int grid = static_cast<int>(std::min<long long>(grid_cap, work));
+  grid = static_cast<int>(std::min<long long>(grid, work));
   fused_sample_kernel<TP, TQ, PROBS><<<grid, FU_THREADS, fu_smem_bytes(), st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "fused sampling launch");
