@@ -219,13 +219,20 @@ struct StatsAcc {
     nA = -AM;
   }
 
+  // warp-wide merge: the max first, then each lane rescales its sum once to
+  // the common offset fl(M*c) and the sums are added
   __device__ __forceinline__ void warp_reduce(float c) {
+    float M = m;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      merge(m2, s2, c);
-    }
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (M == kNegInf) return;   // every lane empty: s == 0 everywhere
+    const float AM = __fmul_rn(M, c);
+    float t = (m == kNegInf) ? 0.f : s * ex2_approx(__fsub_rn(__fmul_rn(m, c), AM));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    m = M;
+    s = t;
+    nA = -AM;
   }
   __device__ __forceinline__ float2 pack() const { return make_float2(m, s); }
   __device__ __forceinline__ void unpack(float2 p) { m = p.x; s = p.y; }

@@ -10,13 +10,17 @@
 //                 CTAs round-robin (no atomics), so the batch is swept roughly
 //                 in sequence order and sequences complete one after another.
 //   residual unit (sequence b, slice j): sum over one slice of the stopping row
-//                 pair of w = max(0, p - q) (p alone for the bonus row).
+//                 pair of w = max(0, p - q) (p alone for the bonus row).  Unit
+//                 r = b * Sr + j is also dealt round-robin (CTA r mod grid); its
+//                 producer takes it as soon as sequence b's scan has published
+//                 the stopping position, ahead of its next sweep unit.
 // Roles inside a CTA (one warp each, plus eight consumer warps):
 //   producer   one thread streams work-item bytes into a 4-stage ring of 16 KB
 //              shared-memory stages with 1-D bulk async copies (cp.async.bulk,
 //              completion counted on an mbarrier per stage) and writes a small
-//              descriptor per stage.  It takes published residual units before
-//              its next sweep unit, so stopping rows are re-read from L2.
+//              descriptor per stage.  Before each sweep unit it checks (with a
+//              load issued one unit ahead) whether the sequence of its next
+//              residual unit is ready, so stopping rows are re-read from L2.
 //   consumers  each of the eight warps reduces its share of every stage, writes
 //              its own partial at the end of a work item and counts it in the
 //              sequence's arrival counter; no CTA-wide barrier is involved.
@@ -24,11 +28,11 @@
 //              finisher warp through a shared-memory queue.
 //   finisher   runs the accept scan of a sequence whose sweep is complete
 //              (warp-parallel merge of the partials, one lane per position),
-//              writes the accepted prefix and publishes the residual units; and
+//              writes the accepted prefix and marks the sequence ready; and
 //              runs the inverse-CDF pick of a sequence whose residual sums are
 //              complete (slice prefix sums, then a warp-wide prefix scan over
 //              the chosen slice, re-read from L2).
-// Every wait (stage barriers, the task queue, residual-queue polling) is
+// Every wait (stage barriers, the task queue, readiness polling) is
 // bounded in time; a timeout sets an error word, and the last CTA to leave then
 // marks every sequence -2.
 #pragma once
@@ -60,7 +64,6 @@ struct SeqInfo {          // per sequence, written by the accept scan
 };
 
 struct FuCtl {                    // zeroed before every call (32 bytes reserved)
-  unsigned long long rq;          // residual queue: low 32 bits reserved, high 32 bits claimed
   unsigned err;                   // a wait timed out
   unsigned done;                  // CTAs that have left
 };
@@ -84,7 +87,7 @@ struct FusedArgs {
   FuCtl* ctl;
   unsigned* cnt1;                // [B] sweep warp-partials completed
   unsigned* cnt2;                // [B] residual warp-partials completed
-  unsigned* queue;               // [B * Sr] residual units: b * FU_MAX_SR + j + 1
+  unsigned* ready;               // [B] 1 once the accept scan has written SeqInfo
   SeqInfo* info;                 // [B]
   double* rpart;                 // [B * Sr * FU_CW] residual warp-partial sums
   float2* part;                  // [U * FU_CW] sweep warp-partials
@@ -403,10 +406,7 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane) {
   }
   __syncwarp();
   __threadfence();
-  unsigned k0 = 0;
-  if (lane == 0) k0 = static_cast<unsigned>(atomicAdd(&a.ctl->rq, static_cast<unsigned long long>(a.Sr)));
-  k0 = __shfl_sync(0xffffffffu, k0, 0);
-  for (int j = lane; j < a.Sr; j += 32) st_release_u32(a.queue + k0 + j, static_cast<unsigned>(b * FU_MAX_SR + j + 1));
+  if (lane == 0) st_release_u32(a.ready + b, 1u);
 }
 
 // ---------------------------------------------------------------------------
@@ -505,16 +505,25 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
     const int k0 = min(n, lane * seg), k1 = min(n, k0 + seg);
     float Tt = 0.f;
     int lastpos = -1;
-    for (int k = k0; k < k1; k += 8) {
-      float zp[8], zq[8];
-      load8_global<TP>(prow + static_cast<long long>(e0 + k) * TP::esz, zp);
-      if (has_q) load8_global<QT>(qrow + static_cast<long long>(e0 + k) * QT::esz, zq);
+    for (int k = k0; k < k1; k += 16) {
+      float zp[2][8], zq[2][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float w = resid_w(zp[i], has_q ? zq[i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q, PROBS);
-        Tt += w;
-        if (w > 0.f) lastpos = e0 + k + i;
-      }
+      for (int v = 0; v < 2; ++v)   // both loads of the pair in flight together
+        if (k + 8 * v < k1) {
+          load8_global<TP>(prow + static_cast<long long>(e0 + k + 8 * v) * TP::esz, zp[v]);
+          if (has_q) load8_global<QT>(qrow + static_cast<long long>(e0 + k + 8 * v) * QT::esz, zq[v]);
+        }
+#pragma unroll
+      for (int v = 0; v < 2; ++v)
+        if (k + 8 * v < k1) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float w = resid_w(zp[v][i], has_q ? zq[v][i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q,
+                                    PROBS);
+            Tt += w;
+            if (w > 0.f) lastpos = e0 + k + 8 * v + i;
+          }
+        }
     }
     double x = static_cast<double>(Tt);
 #pragma unroll
@@ -527,16 +536,25 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
     int cand = 0x7fffffff;
     if (owner) {
       float run = 0.f;
-      for (int k = k0; k < k1 && cand == 0x7fffffff; k += 8) {
-        float zp[8], zq[8];
-        load8_global<TP>(prow + static_cast<long long>(e0 + k) * TP::esz, zp);
-        if (has_q) load8_global<QT>(qrow + static_cast<long long>(e0 + k) * QT::esz, zq);
+      for (int k = k0; k < k1 && cand == 0x7fffffff; k += 16) {
+        float zp[2][8], zq[2][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float w = resid_w(zp[i], has_q ? zq[i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q, PROBS);
-          run += w;
-          if (cand == 0x7fffffff && lb + static_cast<double>(run) > target) cand = e0 + k + i;
-        }
+        for (int v = 0; v < 2; ++v)
+          if (k + 8 * v < k1) {
+            load8_global<TP>(prow + static_cast<long long>(e0 + k + 8 * v) * TP::esz, zp[v]);
+            if (has_q) load8_global<QT>(qrow + static_cast<long long>(e0 + k + 8 * v) * QT::esz, zq[v]);
+          }
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+          if (k + 8 * v < k1) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float w = resid_w(zp[v][i], has_q ? zq[v][i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q,
+                                      PROBS);
+              run += w;
+              if (cand == 0x7fffffff && lb + static_cast<double>(run) > target) cand = e0 + k + 8 * v + i;
+            }
+          }
       }
     }
 #pragma unroll
@@ -577,6 +595,9 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
   const unsigned per_seq = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S);
   const int W = a.K + 1;
   unsigned next_sweep = blockIdx.x;
+  unsigned next_res = blockIdx.x;
+  // readiness of the next residual unit's sequence, loaded one unit ahead
+  unsigned res_ready = next_res < RU ? ld_acquire_u32(a.ready + next_res / a.Sr) : 0u;
 
   auto next_stage = [&]() -> bool {
     if (fu_aborted(sh)) return false;
@@ -592,29 +613,31 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
 
   bool ok = true;
   while (ok) {
-    // a published residual unit first (claimed through one packed word)
-    long long rid = -1;
-    {
-      unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(&a.ctl->rq);
-      for (int tries = 0; tries < 4 && static_cast<unsigned>(v >> 32) < static_cast<unsigned>(v); ++tries) {
-        const unsigned long long prev = atomicCAS(&a.ctl->rq, v, v + (1ull << 32));
-        if (prev == v) { rid = static_cast<long long>(v >> 32); break; }
-        v = prev;
+    long long rid = -1, uid = -1;
+    if (next_res < RU && res_ready) {
+      rid = next_res;
+      next_res += gridDim.x;
+    } else if (next_sweep < a.U) {
+      uid = next_sweep;
+      next_sweep += gridDim.x;
+    } else if (next_res < RU) {
+      // sweep done: wait for the next residual unit's sequence
+      const uint64_t t0 = global_ns();
+      while (ld_acquire_u32(a.ready + next_res / a.Sr) == 0u) {
+        if (fu_aborted(sh) || global_ns() - t0 > a.timeout_ns) break;
+        __nanosleep(200);
       }
-    }
-    long long uid = -1;
-    if (rid < 0) {
-      if (next_sweep < a.U) {
-        uid = next_sweep;
-        next_sweep += gridDim.x;
-      } else {
-        // sweep done: the next residual unit, waiting for its publication
-        const unsigned long long v = atomicAdd(&a.ctl->rq, 1ull << 32);
-        const unsigned r = static_cast<unsigned>(v >> 32);
-        if (r >= RU) break;
-        rid = r;
+      if (ld_acquire_u32(a.ready + next_res / a.Sr) == 0u) {
+        fu_fail(sh, a.ctl, 2u);
+        break;
       }
+      rid = next_res;
+      next_res += gridDim.x;
+    } else {
+      break;
     }
+    // issue the next readiness load now; its latency overlaps this unit's copies
+    res_ready = next_res < RU ? ld_acquire_u32(a.ready + next_res / a.Sr) : 0u;
     if (uid >= 0) {
       const unsigned u = static_cast<unsigned>(uid);
       const int b = static_cast<int>(u / per_seq);
@@ -645,21 +668,9 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
       }
       continue;
     }
-    // residual unit rid: its queue entry is written by the scan that reserved it
-    unsigned ent = ld_acquire_u32(a.queue + rid);
-    if (ent == 0) {
-      const uint64_t t0 = global_ns();
-      while ((ent = ld_acquire_u32(a.queue + rid)) == 0) {
-        if (fu_aborted(sh) || global_ns() - t0 > a.timeout_ns) break;
-        __nanosleep(200);
-      }
-      if (ent == 0) {
-        fu_fail(sh, a.ctl, 2u);
-        break;
-      }
-    }
-    const int b = static_cast<int>((ent - 1) / FU_MAX_SR);
-    const int j = static_cast<int>((ent - 1) % FU_MAX_SR);
+    // residual unit rid = b * Sr + j; sequence b is ready (its SeqInfo is written)
+    const int b = static_cast<int>(rid / a.Sr);
+    const int j = static_cast<int>(rid - static_cast<long long>(b) * a.Sr);
     SeqInfo inf;
     {
       const int* src = reinterpret_cast<const int*>(a.info + b);

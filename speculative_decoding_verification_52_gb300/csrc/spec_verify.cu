@@ -284,7 +284,7 @@ int finish_max_cluster(int dev) {
 }
 
 // Workspace of the fused sampling kernel:
-//   [FuCtl | cnt1[B] | cnt2[B] | queue[B*Sr]]        zeroed per call
+//   [FuCtl | cnt1[B] | cnt2[B] | ready[B]]           zeroed per call
 //   [info[B] | rpart[B*Sr*8] (double) | part[rows*S*8] (float2)]
 struct FusedLayout {
   size_t zero_bytes, info_off, rpart_off, part_off, total;
@@ -292,7 +292,7 @@ struct FusedLayout {
 FusedLayout fused_layout(int B, int K, int V) {
   FusedLayout l{};
   const size_t sr = static_cast<size_t>(max_rslices(V));
-  l.zero_bytes = align_up(32 + 8u * static_cast<size_t>(B) + 4u * static_cast<size_t>(B) * sr, 16);
+  l.zero_bytes = align_up(32 + 12u * static_cast<size_t>(B), 16);
   l.info_off = l.zero_bytes;
   l.rpart_off = align_up(l.info_off + sizeof(SeqInfo) * static_cast<size_t>(B), 16);
   l.part_off = align_up(l.rpart_off + sizeof(double) * FU_CW * static_cast<size_t>(B) * sr, 16);
@@ -379,7 +379,7 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   a.ctl = reinterpret_cast<FuCtl*>(w);
   a.cnt1 = reinterpret_cast<unsigned*>(w + 32);
   a.cnt2 = a.cnt1 + B;
-  a.queue = a.cnt2 + B;
+  a.ready = a.cnt2 + B;
   a.info = reinterpret_cast<SeqInfo*>(w + lay.info_off);
   a.rpart = reinterpret_cast<double*>(w + lay.rpart_off);
   a.part = reinterpret_cast<float2*>(w + lay.part_off);
