@@ -3,38 +3,38 @@
 // exactness rule"; "Speculative decoding: draft, verify, repeat", steps 1-3;
 // "Speculative Decoding: from idea to SOTA", section 3).
 //
-// Work items:
+// Work items (both kinds dealt round-robin to the CTAs, no atomics to claim):
 //   sweep unit    (sequence b, row r, slice j): softmax-normaliser partials
 //                 (max m, sum 2^(z*c - fl(m*c))) of one slice of one target or
-//                 draft row.  Units are numbered sequence-major and dealt to the
-//                 CTAs round-robin (no atomics), so the batch is swept roughly
-//                 in sequence order and sequences complete one after another.
-//   residual unit (sequence b, slice j): sum over one slice of the stopping row
-//                 pair of w = max(0, p - q) (p alone for the bonus row).  Unit
-//                 r = b * Sr + j is also dealt round-robin (CTA r mod grid); its
-//                 producer takes it as soon as sequence b's scan has published
-//                 the stopping position, ahead of its next sweep unit.
-// Roles inside a CTA (one warp each, plus eight consumer warps):
-//   producer   one thread streams work-item bytes into a 4-stage ring of 16 KB
+//                 draft row, numbered sequence-major so the batch is swept in
+//                 roughly sequence order.
+//   residual unit (sequence b, slice j): the residual weights w = max(0, p - q)
+//                 (p alone for the bonus row) of one slice of the stopping row
+//                 pair, summed per block of 256 elements.  A producer takes its
+//                 next residual unit as soon as sequence b is ready (its accept
+//                 scan is done), ahead of its next sweep unit, so the stopping
+//                 rows are re-read while still in L2.
+// Roles inside a CTA:
+//   producer   (1 thread) streams work-item bytes into a 4-stage ring of 16 KB
 //              shared-memory stages with 1-D bulk async copies (cp.async.bulk,
 //              completion counted on an mbarrier per stage) and writes a small
-//              descriptor per stage.  Before each sweep unit it checks (with a
-//              load issued one unit ahead) whether the sequence of its next
-//              residual unit is ready, so stopping rows are re-read from L2.
-//   consumers  each of the eight warps reduces its share of every stage, writes
-//              its own partial at the end of a work item and counts it in the
-//              sequence's arrival counter; no CTA-wide barrier is involved.
-//              The warp whose arrival completes a sequence hands a task to the
-//              finisher warp through a shared-memory queue.
-//   finisher   runs the accept scan of a sequence whose sweep is complete
-//              (warp-parallel merge of the partials, one lane per position),
-//              writes the accepted prefix and marks the sequence ready; and
-//              runs the inverse-CDF pick of a sequence whose residual sums are
-//              complete (slice prefix sums, then a warp-wide prefix scan over
-//              the chosen slice, re-read from L2).
-// Every wait (stage barriers, the task queue, readiness polling) is
-// bounded in time; a timeout sets an error word, and the last CTA to leave then
-// marks every sequence -2.
+//              descriptor per stage.
+//   consumers  (8 warps) each reduce their share of every stage.  At the end of
+//              a work item every warp writes its own partial; the warps count
+//              themselves in shared memory and the last one adds the item to
+//              the sequence's global counter with a fire-and-forget release
+//              reduction.
+//   finisher   (1 warp) owns a fixed set of sequences: the accept scan of b runs
+//              on CTA b mod grid, the pick of b on CTA (b + grid/2) mod grid.
+//              It polls those sequences' counters; the scan merges the partials
+//              (warp-parallel), tests all positions at once (one lane each),
+//              writes the accepted prefix and marks the sequence ready; the
+//              pick finds the 256-element block holding u*R from the block
+//              sums, re-reads that block, and locates the token with a
+//              warp-wide prefix scan.
+// Every wait (stage barriers, readiness and counter polling) is bounded in
+// time; a timeout sets an error word, and the last CTA to leave then marks
+// every sequence -2.
 #pragma once
 
 #include <type_traits>
@@ -49,8 +49,7 @@ constexpr int FU_THREADS = FU_CT + 64;            // + producer warp + finisher 
 constexpr int FU_FIN_WARP = FU_CW + 1;
 constexpr int FU_STAGE = 16384;
 constexpr int FU_NSTAGE = 4;
-constexpr int FU_MAX_SR = 64;                     // residual slices per row (host checks)
-constexpr int FU_TASKQ = 64;                      // finisher task queue capacity
+constexpr int FU_BLK = 256;                       // residual block (elements)
 
 enum : int { KIND_STOP = -1, KIND_SWEEP = 0, KIND_RESID = 1 };
 enum : int { FL_FIRST = 1, FL_LAST = 2, FL_DRAFT = 4, FL_HASQ = 8 };
@@ -63,14 +62,14 @@ struct SeqInfo {          // per sequence, written by the accept scan
   float pad;
 };
 
-struct FuCtl {                    // zeroed before every call (32 bytes reserved)
-  unsigned err;                   // a wait timed out
-  unsigned done;                  // CTAs that have left
+struct FuCtl {            // zeroed before every call (32 bytes reserved)
+  unsigned err;           // a wait timed out
+  unsigned done;          // CTAs that have left
 };
 static_assert(sizeof(FuCtl) <= 32, "control block must fit its 32-byte slot");
 
 struct StageDesc {
-  int kind, b, unit, e0, n, flags, tstar, pad;
+  int kind, b, unit, e0, n, flags, pad0, pad1;
   float AP, AQ, iSp, iSq;
 };
 
@@ -82,14 +81,15 @@ struct FusedArgs {
   int B, K, V, RB;               // RB: sweep rows per sequence (2K+1 logits, K+1 probabilities)
   int S, L;                      // sweep slices per row and their length (elements)
   int Sr, Lr, RE;                // residual slices per row, their length, elements per stage
+  int NB;                        // residual blocks per row = ceil(V / 256)
   unsigned U;                    // sweep units = B * RB * S
   float c;                       // log2(e) / T
   FuCtl* ctl;
-  unsigned* cnt1;                // [B] sweep warp-partials completed
-  unsigned* cnt2;                // [B] residual warp-partials completed
+  unsigned* cnt1;                // [B] sweep units completed
+  unsigned* cnt2;                // [B] residual units completed
   unsigned* ready;               // [B] 1 once the accept scan has written SeqInfo
   SeqInfo* info;                 // [B]
-  double* rpart;                 // [B * Sr * FU_CW] residual warp-partial sums
+  float* bsum;                   // [B * NB] residual block sums
   float2* part;                  // [U * FU_CW] sweep warp-partials
   int32_t* out_tokens;           // [B, K+1]
   int32_t* num_accepted;         // [B]
@@ -104,9 +104,6 @@ struct FuShared {
   uint64_t empty[FU_NSTAGE];
   StageDesc desc[FU_NSTAGE];
   int unit_cnt[FU_NSTAGE];       // consumer warps done with the work item ending in this stage
-  int task[FU_TASKQ];            // (b << 1 | kind) + 1, 0 = empty slot
-  unsigned task_tail;            // next slot to fill (shared-memory atomics)
-  int cons_done;                 // consumer warps that have left
   int abort;
 };
 
@@ -138,8 +135,9 @@ __device__ __forceinline__ void load8_global(const unsigned char* p, float* x) {
   }
 }
 
-// residual weight of one element; the slice sums and the pick use exactly this
-// arithmetic, so both see the same fp32 values
+// residual weight of one element; the block sums and the pick use exactly this
+// arithmetic (and the same 8-element sequential sums), so both see the same
+// fp32 values
 __device__ __forceinline__ float resid_w(float zp, float zq, float c, float nAP, float nAQ, float iSp, float iSq,
                                          bool has_q, bool probs) {
   const float wp = __fmul_rn(ex2_approx(__fmaf_rn(zp, c, nAP)), iSp);
@@ -238,49 +236,65 @@ __device__ __forceinline__ void stats_stage(const uint4* buf, int nvec, int ctid
   else stats_stage_f32(buf, nvec, ctid, c, acc);
 }
 
-// residual partial sum over one stage: P chunk at buf, Q chunk at buf + RE*esz_P
+// Residual weights of one stage (P chunk at buf, Q chunk at buf + RE*esz_P),
+// summed per 256-element block: warp cw covers elements [256*(8k + cw), +256)
+// of the stage in its k-th pass (lane l: 8 consecutive elements), so each
+// block sum is one warp reduction of the lanes' sequential 8-element sums.
 template <class TP, class TQ, bool PROBS>
-__device__ __forceinline__ float resid_stage(const unsigned char* buf, const StageDesc& d, int RE, int ctid, float c) {
+__device__ __forceinline__ void resid_stage(const unsigned char* buf, const StageDesc& d, int RE, int cw, int lane,
+                                            float c, float* bsum_row) {
   using QT = typename std::conditional<PROBS, F32T, TQ>::type;
   const bool has_q = d.flags & FL_HASQ;
   const unsigned char* qb = buf + RE * TP::esz;
-  float acc = 0.f;
-  for (int g = ctid; g < d.n / 8; g += FU_CT) {
-    float zp[8], zq[8];
-    load8_smem<TP>(buf + g * 8 * TP::esz, zp);
-    if (has_q) load8_smem<QT>(qb + g * 8 * QT::esz, zq);
+  const int ngroups = d.n / 8;
+  for (int k = 0; k * FU_CT * 8 < RE; ++k) {
+    const int g0 = FU_CT * k + 32 * cw;   // first 8-element group of this warp's block
+    if (g0 >= ngroups) break;
+    const int g = g0 + lane;
+    float s = 0.f;
+    if (g < ngroups) {
+      float zp[8], zq[8];
+      load8_smem<TP>(buf + g * 8 * TP::esz, zp);
+      if (has_q) load8_smem<QT>(qb + g * 8 * QT::esz, zq);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      acc += resid_w(zp[i], has_q ? zq[i] : 0.f, c, -d.AP, -d.AQ, d.iSp, d.iSq, has_q, PROBS);
+      for (int i = 0; i < 8; ++i) s += resid_w(zp[i], has_q ? zq[i] : 0.f, c, -d.AP, -d.AQ, d.iSp, d.iSq, has_q, PROBS);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) bsum_row[(d.e0 + g0 * 8) / FU_BLK] = s;
   }
-  return acc;
-}
-
-// value of row r held by lanes (row r lives in lane r & 31, register r >> 5)
-template <class T>
-__device__ __forceinline__ T row_get(const T (&v)[2], int r) {
-  const T v0 = __shfl_sync(0xffffffffu, v[0], r & 31);
-  const T v1 = __shfl_sync(0xffffffffu, v[1], r & 31);
-  return r < 32 ? v0 : v1;
 }
 
 // ---------------------------------------------------------------------------
 // finisher: accept scan of sequence b (one warp)
 // ---------------------------------------------------------------------------
+template <class T>
+__device__ __forceinline__ T row_get(const T (&v)[2], int r) {   // row r lives in lane r & 31, slot r >> 5
+  const T v0 = __shfl_sync(0xffffffffu, v[0], r & 31);
+  const T v1 = __shfl_sync(0xffffffffu, v[1], r & 31);
+  return r < 32 ? v0 : v1;
+}
+
 template <class TP, class TQ, bool PROBS>
 __device__ void finish_scan(const FusedArgs& a, int b, int lane) {
   const int K = a.K, W = K + 1, V = a.V;
   const int npart = a.S * FU_CW;
-  // merge each row's S x 8 warp partials with the whole warp (rows in groups
-  // of 8, all loads of a group in flight together); row r ends up in lane
-  // r & 31, register r >> 5
+  // per-position inputs first (independent loads, in flight with the merge)
+  int x = -1;
+  float u0 = 0.f;
+  if (lane < K) {
+    x = a.tokens[static_cast<long long>(b) * K + lane];
+    u0 = a.uni[(static_cast<long long>(b) * W + lane) * 2];
+  }
+  // merge each row's S x 8 warp partials with the whole warp, four rows at a
+  // time with all their loads in flight; row r ends up in lane r & 31, slot r >> 5
   float Ar[2] = {0.f, 0.f};
   double Sr[2] = {0.0, 0.0};
   int st[2] = {1, 1};
-  for (int r0 = 0; r0 < a.RB; r0 += 8) {
-    float2 pv[8][2];
+  for (int r0 = 0; r0 < a.RB; r0 += 4) {
+    float2 pv[4][2];
 #pragma unroll
-    for (int g = 0; g < 8; ++g)
+    for (int g = 0; g < 4; ++g)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int r = r0 + g, i = lane + 32 * h;
@@ -288,21 +302,21 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane) {
                                             : make_float2(kNegInf, 0.f);
       }
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
+    for (int g = 0; g < 4; ++g) {
       const int r = r0 + g;
       if (r >= a.RB) break;
-      // partials beyond 64 per row (small batches with many slices)
+      const float2* rowp = a.part + (static_cast<long long>(b) * a.RB + r) * npart;
       float M = kNegInf;
       bool poison = false;
-      for (int i = 64 + lane; i < npart; i += 32) {
-        const float2 p = __ldcg(a.part + (static_cast<long long>(b) * a.RB + r) * npart + i);
-        if (p.x != p.x) poison = true;
-        else M = fmaxf(M, p.x);
-      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         if (pv[g][h].x != pv[g][h].x) poison = true;
         else M = fmaxf(M, pv[g][h].x);
+      }
+      for (int i = 64 + lane; i < npart; i += 32) {   // rows with more than 64 partials
+        const float2 p = __ldcg(rowp + i);
+        if (p.x != p.x) poison = true;
+        else M = fmaxf(M, p.x);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -316,7 +330,7 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane) {
           if (pv[g][h].x != kNegInf)
             acc += static_cast<double>(pv[g][h].y) * static_cast<double>(exp2f(__fmul_rn(pv[g][h].x, a.c) - AM));
         for (int i = 64 + lane; i < npart; i += 32) {
-          const float2 p = __ldcg(a.part + (static_cast<long long>(b) * a.RB + r) * npart + i);
+          const float2 p = __ldcg(rowp + i);
           if (p.x != kNegInf) acc += static_cast<double>(p.y) * static_cast<double>(exp2f(__fmul_rn(p.x, a.c) - AM));
         }
 #pragma unroll
@@ -338,30 +352,26 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane) {
   const float At = row_get(Ar, rp), Aq = row_get(Ar, rq);
   const double St = row_get(Sr, rp), Sq = row_get(Sr, rq);
   const int stt = row_get(st, rp), stq = row_get(st, rq);
-  int x = -1;
   bool tok_bad = false, acc_t = true;
-  int row_bad = 0;   // 0 ok, 1 invalid, 2 poisoned (rows read at position t)
+  int row_bad = 0;   // rows read at position t: 0 ok, 1 invalid, 2 poisoned
   if (t < K) {
-    x = a.tokens[static_cast<long long>(b) * K + t];
     tok_bad = x < 0 || x >= V;
     row_bad = stt;
     if (!PROBS && row_bad == 0) row_bad = stq;
     if (!tok_bad && row_bad == 0) {
       const double cd = static_cast<double>(a.c);
-      const double zp = static_cast<double>(TP::load(a.target, (static_cast<long long>(b) * W + t) * V + x));
-      const double pa = exp2_d(zp * cd - static_cast<double>(At)) / St;
-      double qc;
       const long long oq = (static_cast<long long>(b) * K + t) * V + x;
+      const float zpf = TP::load(a.target, (static_cast<long long>(b) * W + t) * V + x);
+      const float zqf = PROBS ? F32T::load(a.draft, oq) : TQ::load(a.draft, oq);
+      const double pa = exp2_d(static_cast<double>(zpf) * cd - static_cast<double>(At)) / St;
+      double qc;
       if (PROBS) {
-        const float qv = F32T::load(a.draft, oq);
-        if (qv != qv || qv < 0.f) row_bad = 1;
-        qc = static_cast<double>(qv);
+        if (zqf != zqf || zqf < 0.f) row_bad = 1;
+        qc = static_cast<double>(zqf);
       } else {
-        const double zq = static_cast<double>(TQ::load(a.draft, oq));
-        qc = exp2_d(zq * cd - static_cast<double>(Aq)) / Sq;
+        qc = exp2_d(static_cast<double>(zqf) * cd - static_cast<double>(Aq)) / Sq;
       }
-      const double u = static_cast<double>(a.uni[(static_cast<long long>(b) * W + t) * 2]);
-      acc_t = (qc == 0.0) || (u < pa / qc);
+      acc_t = (qc == 0.0) || (static_cast<double>(u0) < pa / qc);
     }
   }
   const unsigned badtok = __ballot_sync(0xffffffffu, t < K && tok_bad);
@@ -386,9 +396,11 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane) {
   const float Aq2 = row_get(Ar, has_q ? W + tstar : 0);
   const double Sq2 = row_get(Sr, has_q ? W + tstar : 0);
 
+  // accepted prefix (slot tstar is written by the pick), -1 padding
   int32_t* out = a.out_tokens + static_cast<long long>(b) * W;
+  const int x_all = x;
   for (int j = lane; j < W; j += 32) {
-    const int xj = (j < K) ? a.tokens[static_cast<long long>(b) * K + j] : -1;
+    const int xj = (j < 32) ? x_all : a.tokens[static_cast<long long>(b) * K + j];
     out[j] = (status == 0 && j < tstar) ? xj : -1;
   }
   if (lane == 0) {
@@ -415,7 +427,7 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane) {
 template <class TP, class TQ, bool PROBS>
 __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
   using QT = typename std::conditional<PROBS, F32T, TQ>::type;
-  const int K = a.K, W = K + 1, V = a.V;
+  const int K = a.K, W = K + 1, V = a.V, NB = a.NB;
   SeqInfo inf;
   {
     const int* src = reinterpret_cast<const int*>(a.info + b);
@@ -424,139 +436,114 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
     for (int i = 0; i < 8; ++i) dst[i] = __ldcg(src + i);
   }
   if (inf.status != 0) return;   // outputs already written by the scan
-  const bool has_q0 = inf.tstar < K;
   const unsigned char* prow = a.target + (static_cast<long long>(b) * W + inf.tstar) * V * TP::esz;
-  const unsigned char* qrow = has_q0 ? a.draft + (static_cast<long long>(b) * K + inf.tstar) * V * QT::esz : nullptr;
+  const unsigned char* qrow =
+      inf.tstar < K ? a.draft + (static_cast<long long>(b) * K + inf.tstar) * V * QT::esz : nullptr;
+  float* brow = a.bsum + static_cast<long long>(b) * NB;
+  bool has_q = inf.tstar < K;
   const float c = a.c;
-  // slice sums (lanes own slices lane and lane + 32)
-  double sl[2] = {0.0, 0.0};
+  const int nbl = (NB + 31) / 32;               // blocks per lane (contiguous)
+  const int bl0 = min(NB, lane * nbl), bl1 = min(NB, bl0 + nbl);
+
+  auto weights8 = [&](int e, float* w) {   // w of the 8 elements at e (e % 8 == 0)
+    float zp[8], zq[8];
+    load8_global<TP>(prow + static_cast<long long>(e) * TP::esz, zp);
+    if (has_q) load8_global<QT>(qrow + static_cast<long long>(e) * QT::esz, zq);
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int j = lane + 32 * h;
-    if (j < a.Sr) {
-      const double* rp = a.rpart + (static_cast<long long>(b) * a.Sr + j) * FU_CW;
-      double s = 0.0;
-#pragma unroll
-      for (int w = 0; w < FU_CW; ++w) s += __ldcg(rp + w);
-      sl[h] = s;
-    }
-  }
-  bool has_q = has_q0;
-  double R = 0.0;
+    for (int i = 0; i < 8; ++i)
+      w[i] = resid_w(zp[i], has_q ? zq[i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q, PROBS);
+  };
+
+  double lsum = 0.0, R = 0.0;
   for (int pass = 0; pass < 2; ++pass) {
-    double tot = sl[0] + sl[1];
+    lsum = 0.0;
+    for (int k = bl0; k < bl1; ++k) lsum += static_cast<double>(__ldcg(brow + k));
+    R = lsum;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    R = tot;
+    for (int o = 16; o > 0; o >>= 1) R += __shfl_xor_sync(0xffffffffu, R, o);
     if (R > 0.0 || !has_q) break;
-    // residual mass zero: draw from p_t instead (recompute the slice sums)
+    // residual mass zero: draw from p_t instead (rebuild the block sums; rare)
     has_q = false;
-    sl[0] = sl[1] = 0.0;
-    for (int j = 0; j < a.Sr; ++j) {
-      const int e0 = j * a.Lr, e1 = min(V, e0 + a.Lr);
-      float acc = 0.f;
-      for (int g = e0 / 8 + lane; g < e1 / 8; g += 32) {
-        float zp[8];
-        load8_global<TP>(prow + static_cast<long long>(g) * 8 * TP::esz, zp);
+    for (int blk = 0; blk < NB; ++blk) {
+      const int e = blk * FU_BLK + 8 * lane;
+      float s = 0.f;
+      if (e < V) {
+        float w[8];
+        weights8(e, w);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc += resid_w(zp[i], 0.f, c, -inf.AP, 0.f, inf.iSp, 1.f, false, PROBS);
+        for (int i = 0; i < 8; ++i) s += w[i];
       }
-      double v = static_cast<double>(acc);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if ((j & 31) == lane) sl[j >> 5] = v;
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) brow[blk] = s;
     }
+    __syncwarp();
+    __threadfence_block();
   }
   const double target = static_cast<double>(inf.u1) * R;
-  // slice holding the target: inclusive prefix over slices (lane order, then +32)
-  double pre0 = sl[0];
+  // exclusive prefix of the lanes' block ranges, then the block holding the target
+  double incl = lsum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, pre0, o);
-    if (lane >= o) pre0 += y;
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
-  const double tot0 = __shfl_sync(0xffffffffu, pre0, 31);
-  double pre1 = sl[1];
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, pre1, o);
-    if (lane >= o) pre1 += y;
-  }
-  pre1 += tot0;
-  const unsigned hit0 = __ballot_sync(0xffffffffu, sl[0] > 0.0 && pre0 > target);
-  const unsigned hit1 = __ballot_sync(0xffffffffu, sl[1] > 0.0 && pre1 > target);
-  const unsigned pos0 = __ballot_sync(0xffffffffu, sl[0] > 0.0);
-  const unsigned pos1 = __ballot_sync(0xffffffffu, sl[1] > 0.0);
-  int js;
-  if (hit0) js = __ffs(hit0) - 1;
-  else if (hit1) js = 32 + __ffs(hit1) - 1;
-  else if (pos1) js = 32 + 31 - __clz(pos1);   // rounding: the last slice with mass
-  else if (pos0) js = 31 - __clz(pos0);
-  else js = -1;
-  int pick = -1;
-  if (js >= 0) {
-    const double ex0 = __shfl_sync(0xffffffffu, pre0 - sl[0], js & 31);
-    const double ex1 = __shfl_sync(0xffffffffu, pre1 - sl[1], js & 31);
-    const double base = js < 32 ? ex0 : ex1;
-    const int e0 = js * a.Lr;
-    const int n = min(V, e0 + a.Lr) - e0;
-    int seg = (n + 31) / 32;
-    seg = (seg + 7) / 8 * 8;
-    const int k0 = min(n, lane * seg), k1 = min(n, k0 + seg);
-    float Tt = 0.f;
-    int lastpos = -1;
-    for (int k = k0; k < k1; k += 16) {
-      float zp[2][8], zq[2][8];
-#pragma unroll
-      for (int v = 0; v < 2; ++v)   // both loads of the pair in flight together
-        if (k + 8 * v < k1) {
-          load8_global<TP>(prow + static_cast<long long>(e0 + k + 8 * v) * TP::esz, zp[v]);
-          if (has_q) load8_global<QT>(qrow + static_cast<long long>(e0 + k + 8 * v) * QT::esz, zq[v]);
-        }
-#pragma unroll
-      for (int v = 0; v < 2; ++v)
-        if (k + 8 * v < k1) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float w = resid_w(zp[v][i], has_q ? zq[v][i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q,
-                                    PROBS);
-            Tt += w;
-            if (w > 0.f) lastpos = e0 + k + 8 * v + i;
-          }
-        }
+  int jb = -1, jlast = -1;
+  double jbase = 0.0, lastbase = 0.0;
+  {
+    double run = incl - lsum;
+    for (int k = bl0; k < bl1; ++k) {
+      const double v = static_cast<double>(__ldcg(brow + k));
+      if (v > 0.0) {
+        jlast = k;
+        lastbase = run;
+        if (jb < 0 && run + v > target) { jb = k; jbase = run; }
+      }
+      run += v;
     }
-    double x = static_cast<double>(Tt);
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, jb >= 0);
+  const unsigned pos = __ballot_sync(0xffffffffu, jlast >= 0);
+  int src_lane;
+  bool exact = true;
+  if (hit) src_lane = __ffs(hit) - 1;
+  else if (pos) { src_lane = 31 - __clz(pos); exact = false; }   // rounding: last block with mass
+  else src_lane = -1;
+  int pick = -1;
+  if (src_lane >= 0) {
+    const int blk = __shfl_sync(0xffffffffu, exact ? jb : jlast, src_lane);
+    const double bb = __shfl_sync(0xffffffffu, exact ? jbase : lastbase, src_lane);
+    // re-read the block: lane l holds elements blk*256 + 8l .. +8
+    const int e = blk * FU_BLK + 8 * lane;
+    float w[8];
+    float s = 0.f;
+    if (e < V) {
+      weights8(e, w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += w[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = 0.f;
+    }
+    double x2 = static_cast<double>(s);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+      const double y = __shfl_up_sync(0xffffffffu, x2, o);
+      if (lane >= o) x2 += y;
     }
-    const double lb = base + (x - static_cast<double>(Tt));
-    const bool owner = Tt > 0.f && lb <= target && lb + static_cast<double>(Tt) > target;
-    int cand = 0x7fffffff;
-    if (owner) {
+    const double lb = bb + (x2 - static_cast<double>(s));
+    int cand = 0x7fffffff, lastpos = -1;
+    if (s > 0.f && lb <= target && lb + static_cast<double>(s) > target) {
       float run = 0.f;
-      for (int k = k0; k < k1 && cand == 0x7fffffff; k += 16) {
-        float zp[2][8], zq[2][8];
 #pragma unroll
-        for (int v = 0; v < 2; ++v)
-          if (k + 8 * v < k1) {
-            load8_global<TP>(prow + static_cast<long long>(e0 + k + 8 * v) * TP::esz, zp[v]);
-            if (has_q) load8_global<QT>(qrow + static_cast<long long>(e0 + k + 8 * v) * QT::esz, zq[v]);
-          }
-#pragma unroll
-        for (int v = 0; v < 2; ++v)
-          if (k + 8 * v < k1) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float w = resid_w(zp[v][i], has_q ? zq[v][i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q,
-                                      PROBS);
-              run += w;
-              if (cand == 0x7fffffff && lb + static_cast<double>(run) > target) cand = e0 + k + 8 * v + i;
-            }
-          }
+      for (int i = 0; i < 8; ++i) {
+        run += w[i];
+        if (cand == 0x7fffffff && lb + static_cast<double>(run) > target) cand = e + i;
       }
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (w[i] > 0.f) lastpos = e + i;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
@@ -566,15 +553,11 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
   }
   if (lane == 0) a.out_tokens[static_cast<long long>(b) * W + inf.tstar] = pick;
   if (b == a.debug_b && R > 0.0) {
-    for (int g = lane; g < V / 8; g += 32) {
-      float zp[8], zq[8];
-      load8_global<TP>(prow + static_cast<long long>(g) * 8 * TP::esz, zp);
-      if (has_q) load8_global<QT>(qrow + static_cast<long long>(g) * 8 * QT::esz, zq);
+    for (int e = 8 * lane; e < V; e += 256) {
+      float w[8];
+      weights8(e, w);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float w = resid_w(zp[i], has_q ? zq[i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q, PROBS);
-        a.debug_row[g * 8 + i] = static_cast<float>(static_cast<double>(w) / R);
-      }
+      for (int i = 0; i < 8; ++i) a.debug_row[e + i] = static_cast<float>(static_cast<double>(w[i]) / R);
     }
     if (lane == 0) *a.debug_mass = static_cast<float>(R);
   }
@@ -596,8 +579,9 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
   const int W = a.K + 1;
   unsigned next_sweep = blockIdx.x;
   unsigned next_res = blockIdx.x;
-  // readiness of the next residual unit's sequence, loaded one unit ahead
-  unsigned res_ready = next_res < RU ? ld_acquire_u32(a.ready + next_res / a.Sr) : 0u;
+  // readiness of the next residual unit's sequence: relaxed loads, issued one
+  // unit ahead so their latency overlaps the copies
+  unsigned res_ready = next_res < RU ? ld_relaxed_u32(a.ready + next_res / a.Sr) : 0u;
 
   auto next_stage = [&]() -> bool {
     if (fu_aborted(sh)) return false;
@@ -623,11 +607,12 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
     } else if (next_res < RU) {
       // sweep done: wait for the next residual unit's sequence
       const uint64_t t0 = global_ns();
-      while (ld_acquire_u32(a.ready + next_res / a.Sr) == 0u) {
+      bool rdy = false;
+      while (!(rdy = ld_relaxed_u32(a.ready + next_res / a.Sr) != 0u)) {
         if (fu_aborted(sh) || global_ns() - t0 > a.timeout_ns) break;
         __nanosleep(200);
       }
-      if (ld_acquire_u32(a.ready + next_res / a.Sr) == 0u) {
+      if (!rdy) {
         fu_fail(sh, a.ctl, 2u);
         break;
       }
@@ -636,8 +621,7 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
     } else {
       break;
     }
-    // issue the next readiness load now; its latency overlaps this unit's copies
-    res_ready = next_res < RU ? ld_acquire_u32(a.ready + next_res / a.Sr) : 0u;
+    res_ready = next_res < RU ? ld_relaxed_u32(a.ready + next_res / a.Sr) : 0u;
     if (uid >= 0) {
       const unsigned u = static_cast<unsigned>(uid);
       const int b = static_cast<int>(u / per_seq);
@@ -668,7 +652,8 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
       }
       continue;
     }
-    // residual unit rid = b * Sr + j; sequence b is ready (its SeqInfo is written)
+    // residual unit rid = b * Sr + j of a ready sequence
+    __threadfence();   // acquire side of the readiness flag: SeqInfo is visible
     const int b = static_cast<int>(rid / a.Sr);
     const int j = static_cast<int>(rid - static_cast<long long>(b) * a.Sr);
     SeqInfo inf;
@@ -679,7 +664,7 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
       for (int i = 0; i < 8; ++i) dst[i] = __ldcg(src + i);
     }
     if (inf.status != 0) {
-      // invalid sequence: a data-less stage, so the arrivals are still counted
+      // invalid sequence: a data-less stage, so the arrival is still counted
       if (!next_stage()) break;
       StageDesc& d = sh.desc[stage];
       d.kind = KIND_RESID;
@@ -708,7 +693,6 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
       d.e0 = e;
       d.n = n;   // elements for residual stages
       d.flags = (e == e0 ? FL_FIRST : 0) | (e + n >= e1 ? FL_LAST : 0) | (has_q ? FL_HASQ : 0);
-      d.tstar = inf.tstar;
       d.AP = inf.AP;
       d.AQ = inf.AQ;
       d.iSp = inf.iSp;
@@ -744,13 +728,10 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
 template <class TP, class TQ, bool PROBS>
 __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& sh, int cw, int lane) {
   const int ctid = cw * 32 + lane;
-  const unsigned per_seq = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S);
-  const unsigned per_res = static_cast<unsigned>(a.Sr);
   int stage = 0;
   uint32_t phase = 0;
   StatsAcc sacc;
   sacc.init();
-  float racc = 0.f;
   for (;;) {
     if (__any_sync(0xffffffffu, fu_aborted(sh))) break;
     if (!__all_sync(0xffffffffu, mbar_wait(&sh.full[stage], phase, a.timeout_ns))) {
@@ -759,10 +740,7 @@ __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& s
     }
     const StageDesc d = sh.desc[stage];
     if (d.kind == KIND_STOP) break;
-    if (d.flags & FL_FIRST) {
-      sacc.init();
-      racc = 0.f;
-    }
+    if (d.flags & FL_FIRST) sacc.init();
     const int cur = stage;
     const unsigned char* buf = ring + stage * FU_STAGE;
     if (d.kind == KIND_SWEEP) {
@@ -772,7 +750,7 @@ __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& s
         stats_stage<TP>(reinterpret_cast<const uint4*>(buf), d.n >> 4, ctid, a.c, sacc);
       }
     } else if (d.n > 0) {
-      racc += resid_stage<TP, TQ, PROBS>(buf, d, a.RE, ctid, a.c);
+      resid_stage<TP, TQ, PROBS>(buf, d, a.RE, cw, lane, a.c, a.bsum + static_cast<long long>(d.b) * a.NB);
     }
     if (++stage == FU_NSTAGE) { stage = 0; phase ^= 1u; }
     if (!(d.flags & FL_LAST)) {
@@ -780,89 +758,71 @@ __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& s
       if (lane == 0) mbar_arrive(&sh.empty[cur]);
       continue;
     }
-
-    // End of a work item: this warp writes its partial; the CTA counts its
-    // warps in shared memory, and the last one counts the item in the
-    // sequence's global arrival counter (one global atomic per item).
-    int task = 0;
-    if (d.kind == KIND_SWEEP) {
-      sacc.warp_reduce(a.c);
-    } else {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) racc += __shfl_xor_sync(0xffffffffu, racc, o);
-    }
+    // End of a work item: every warp writes its partial; the warps count
+    // themselves in shared memory and the last one adds the item to the
+    // sequence's counter (fire-and-forget, release ordered).
+    if (d.kind == KIND_SWEEP) sacc.warp_reduce(a.c);
+    else __syncwarp();
     if (lane == 0) {
       if (d.kind == KIND_SWEEP) a.part[static_cast<long long>(d.unit) * FU_CW + cw] = sacc.pack();
-      else a.rpart[(static_cast<long long>(d.b) * a.Sr + d.unit) * FU_CW + cw] = static_cast<double>(racc);
       __threadfence_block();
       const int prev = atomicAdd(&sh.unit_cnt[cur], 1);
       if (prev == FU_CW - 1) {
         sh.unit_cnt[cur] = 0;   // the slot's next item starts only after this warp releases it
         __threadfence();
-        if (d.kind == KIND_SWEEP) {
-          const unsigned old = atomicAdd(&a.cnt1[d.b], 1u);
-          if (old + 1u == per_seq) task = (d.b << 1 | 0) + 1;
-        } else {
-          const unsigned old = atomicAdd(&a.cnt2[d.b], 1u);
-          if (old + 1u == per_res) task = (d.b << 1 | 1) + 1;
-        }
+        red_release_add_u32(d.kind == KIND_SWEEP ? a.cnt1 + d.b : a.cnt2 + d.b, 1u);
       }
       mbar_arrive(&sh.empty[cur]);
     }
-    if (lane == 0 && task) {
-      __threadfence();
-      // hand the finished sequence to the finisher warp (bounded wait for space)
-      const unsigned slot = atomicAdd(&sh.task_tail, 1u);
-      volatile int* q = reinterpret_cast<volatile int*>(&sh.task[slot % FU_TASKQ]);
-      const uint64_t t0 = global_ns();
-      while (*q != 0) {
-        if (global_ns() - t0 > a.timeout_ns) { fu_fail(sh, a.ctl, 16u); break; }
-        __nanosleep(100);
-      }
-      *q = task;
-    }
     __syncwarp();
   }
-  __syncwarp();
-  if (lane == 0) atomicAdd(&sh.cons_done, 1);
 }
 
 // ---------------------------------------------------------------------------
-// finisher (one warp): takes tasks from the CTA's queue until the consumers
-// have left and the queue is empty
+// finisher (one warp): the scans of sequences b = blockIdx (mod grid) and the
+// picks of sequences b = blockIdx + grid - grid/2 (mod grid), each started as
+// soon as the sequence's counter is complete
 // ---------------------------------------------------------------------------
 template <class TP, class TQ, bool PROBS>
 __device__ void fu_finisher(const FusedArgs& a, FuShared& sh, int lane) {
-  unsigned head = 0;
-  uint64_t idle_since = global_ns();
-  for (;;) {
-    int task = 0;
-    if (lane == 0) task = *reinterpret_cast<volatile int*>(&sh.task[head % FU_TASKQ]);
-    task = __shfl_sync(0xffffffffu, task, 0);
-    if (task != 0) {
-      if (lane == 0) *reinterpret_cast<volatile int*>(&sh.task[head % FU_TASKQ]) = 0;
-      ++head;
-      __threadfence();
-      const int b = (task - 1) >> 1;
-      if (((task - 1) & 1) == 0) finish_scan<TP, TQ, PROBS>(a, b, lane);
-      else finish_pick<TP, TQ, PROBS>(a, b, lane);
-      __syncwarp();
-      idle_since = global_ns();
+  const unsigned G = gridDim.x;
+  const unsigned per_seq = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S);
+  unsigned bs = blockIdx.x;                              // next scan
+  unsigned bp = (blockIdx.x + G - G / 2) % G;            // next pick
+  uint64_t last_progress = global_ns();
+  while (bs < static_cast<unsigned>(a.B) || bp < static_cast<unsigned>(a.B)) {
+    bool progress = false;
+    if (bs < static_cast<unsigned>(a.B)) {
+      unsigned v = 0;
+      if (lane == 0) v = ld_relaxed_u32(a.cnt1 + bs);
+      if (__shfl_sync(0xffffffffu, v, 0) == per_seq) {
+        __threadfence();
+        finish_scan<TP, TQ, PROBS>(a, static_cast<int>(bs), lane);
+        bs += G;
+        progress = true;
+      }
+    }
+    if (bp < static_cast<unsigned>(a.B)) {
+      unsigned v = 0;
+      if (lane == 0) v = ld_relaxed_u32(a.cnt2 + bp);
+      if (__shfl_sync(0xffffffffu, v, 0) == static_cast<unsigned>(a.Sr)) {
+        __threadfence();
+        finish_pick<TP, TQ, PROBS>(a, static_cast<int>(bp), lane);
+        bp += G;
+        progress = true;
+      }
+    }
+    __syncwarp();
+    if (progress) {
+      last_progress = global_ns();
       continue;
     }
-    int done = 0;
-    if (lane == 0) {
-      const int cd = *reinterpret_cast<volatile int*>(&sh.cons_done);
-      const unsigned tail = *reinterpret_cast<volatile unsigned*>(&sh.task_tail);
-      done = (cd == FU_CW && tail == head) || fu_aborted(sh);
-    }
-    if (__shfl_sync(0xffffffffu, done, 0)) break;
-    // bounded: the consumers' own waits end (and they leave) well before this
-    if (global_ns() - idle_since > 4 * a.timeout_ns) {
+    const bool stop = __any_sync(0xffffffffu, fu_aborted(sh) || global_ns() - last_progress > 4 * a.timeout_ns);
+    if (stop) {
       if (lane == 0) fu_fail(sh, a.ctl, 32u);
       break;
     }
-    __nanosleep(128);
+    __nanosleep(256);
   }
 }
 
@@ -881,11 +841,8 @@ __global__ void __launch_bounds__(FU_THREADS, 3) fused_sample_kernel(const Fused
     for (int s = 0; s < FU_NSTAGE; ++s) {
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], FU_CW);
+      sh.unit_cnt[s] = 0;
     }
-    for (int i = 0; i < FU_TASKQ; ++i) sh.task[i] = 0;
-    for (int i = 0; i < FU_NSTAGE; ++i) sh.unit_cnt[i] = 0;
-    sh.task_tail = 0;
-    sh.cons_done = 0;
     sh.abort = 0;
     mbar_fence_init();
   }

@@ -48,8 +48,6 @@ constexpr int kMaxDevices = 64;
 constexpr unsigned long long kWaitNs = 1000000000ull;   // bounded waits: 1 s
 
 int max_slices(int V) { return std::max(1, (V + kMinSlice - 1) / kMinSlice); }
-// residual slices of the fused sampling kernel: >= 4096 elements, at most 64 per row
-int max_rslices(int V) { return std::min(64, std::max(1, (V + 4095) / 4096)); }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -284,18 +282,18 @@ int finish_max_cluster(int dev) {
 }
 
 // Workspace of the fused sampling kernel:
-//   [FuCtl | cnt1[B] | cnt2[B] | ready[B]]           zeroed per call
-//   [info[B] | rpart[B*Sr*8] (double) | part[rows*S*8] (float2)]
+//   [FuCtl | cnt1[B] | cnt2[B] | ready[B]]              zeroed per call
+//   [info[B] | bsum[B * ceil(V/256)] | part[rows * S * 8]]
 struct FusedLayout {
-  size_t zero_bytes, info_off, rpart_off, part_off, total;
+  size_t zero_bytes, info_off, bsum_off, part_off, total;
 };
 FusedLayout fused_layout(int B, int K, int V) {
   FusedLayout l{};
-  const size_t sr = static_cast<size_t>(max_rslices(V));
+  const size_t nb = static_cast<size_t>((V + FU_BLK - 1) / FU_BLK);
   l.zero_bytes = align_up(32 + 12u * static_cast<size_t>(B), 16);
   l.info_off = l.zero_bytes;
-  l.rpart_off = align_up(l.info_off + sizeof(SeqInfo) * static_cast<size_t>(B), 16);
-  l.part_off = align_up(l.rpart_off + sizeof(double) * FU_CW * static_cast<size_t>(B) * sr, 16);
+  l.bsum_off = align_up(l.info_off + sizeof(SeqInfo) * static_cast<size_t>(B), 16);
+  l.part_off = align_up(l.bsum_off + sizeof(float) * static_cast<size_t>(B) * nb, 16);
   const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(2 * K + 1);
   l.total = align_up(l.part_off + rows * static_cast<size_t>(max_slices(V)) * FU_CW * sizeof(float2), 256);
   return l;
@@ -352,11 +350,9 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
     if (gcd(static_cast<long long>(RB) * S, g) == 1) { grid = g; found = true; }
   const long long U = rows * S;
   if (U >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "batch too large for one call");
-  const int RE = (TP::esz == 2 && QE == 2) ? 4096 : 2048;
-  int Lr = 2 * RE;
-  if (ceil_div(V, Lr) > FU_MAX_SR) Lr = ceil_div(ceil_div(V, FU_MAX_SR), RE) * RE;
+  const int RE = (TP::esz == 2 && QE == 2) ? 4096 : 2048;   // residual stage: 16 KB of P+Q at most
+  const int Lr = 2 * RE;
   const int Sr = ceil_div(V, Lr);
-  if (Sr > max_rslices(V)) return fail(SPEC_ERR_UNSUPPORTED, "V=%d too large", V);
 
   const FusedLayout lay = fused_layout(B, K, V);
   unsigned char* w = static_cast<unsigned char*>(ws);
@@ -376,12 +372,13 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   a.RE = RE;
   a.U = static_cast<unsigned>(U);
   a.c = c;
+  a.NB = ceil_div(V, FU_BLK);
   a.ctl = reinterpret_cast<FuCtl*>(w);
   a.cnt1 = reinterpret_cast<unsigned*>(w + 32);
   a.cnt2 = a.cnt1 + B;
   a.ready = a.cnt2 + B;
   a.info = reinterpret_cast<SeqInfo*>(w + lay.info_off);
-  a.rpart = reinterpret_cast<double*>(w + lay.rpart_off);
+  a.bsum = reinterpret_cast<float*>(w + lay.bsum_off);
   a.part = reinterpret_cast<float2*>(w + lay.part_off);
   a.out_tokens = out;
   a.num_accepted = nacc;
