@@ -275,17 +275,37 @@ __device__ __forceinline__ T row_get(const T (&v)[2], int r) {   // row r lives 
   return r < 32 ? v0 : v1;
 }
 
+// Inputs of position `lane` of sequence b that do not depend on the sweep:
+// the drafted token, its target and draft logits (or draft probability) and
+// the accept uniform.  The finisher loads them while it waits for the
+// sequence's sweep to complete.
+struct ScanInputs {
+  int x;
+  float zp, zq, u0;
+};
+
 template <class TP, class TQ, bool PROBS>
-__device__ void finish_scan(const FusedArgs& a, int b, int lane) {
+__device__ __forceinline__ ScanInputs scan_inputs(const FusedArgs& a, int b, int lane) {
+  const int K = a.K, W = K + 1, V = a.V;
+  ScanInputs in{-1, 0.f, 0.f, 0.f};
+  if (lane < K) {
+    in.x = a.tokens[static_cast<long long>(b) * K + lane];
+    in.u0 = a.uni[(static_cast<long long>(b) * W + lane) * 2];
+    if (in.x >= 0 && in.x < V) {
+      const long long oq = (static_cast<long long>(b) * K + lane) * V + in.x;
+      in.zp = TP::load(a.target, (static_cast<long long>(b) * W + lane) * V + in.x);
+      in.zq = PROBS ? F32T::load(a.draft, oq) : TQ::load(a.draft, oq);
+    }
+  }
+  return in;
+}
+
+template <class TP, class TQ, bool PROBS>
+__device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInputs& in) {
   const int K = a.K, W = K + 1, V = a.V;
   const int npart = a.S * FU_CW;
-  // per-position inputs first (independent loads, in flight with the merge)
-  int x = -1;
-  float u0 = 0.f;
-  if (lane < K) {
-    x = a.tokens[static_cast<long long>(b) * K + lane];
-    u0 = a.uni[(static_cast<long long>(b) * W + lane) * 2];
-  }
+  const int x = in.x;
+  const float u0 = in.u0;
   // merge each row's S x 8 warp partials with the whole warp, four rows at a
   // time with all their loads in flight; row r ends up in lane r & 31, slot r >> 5
   float Ar[2] = {0.f, 0.f};
@@ -360,9 +380,7 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane) {
     if (!PROBS && row_bad == 0) row_bad = stq;
     if (!tok_bad && row_bad == 0) {
       const double cd = static_cast<double>(a.c);
-      const long long oq = (static_cast<long long>(b) * K + t) * V + x;
-      const float zpf = TP::load(a.target, (static_cast<long long>(b) * W + t) * V + x);
-      const float zqf = PROBS ? F32T::load(a.draft, oq) : TQ::load(a.draft, oq);
+      const float zpf = in.zp, zqf = in.zq;
       const double pa = exp2_d(static_cast<double>(zpf) * cd - static_cast<double>(At)) / St;
       double qc;
       if (PROBS) {
@@ -789,6 +807,8 @@ __device__ void fu_finisher(const FusedArgs& a, FuShared& sh, int lane) {
   const unsigned per_seq = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S);
   unsigned bs = blockIdx.x;                              // next scan
   unsigned bp = (blockIdx.x + G - G / 2) % G;            // next pick
+  ScanInputs in{};
+  if (bs < static_cast<unsigned>(a.B)) in = scan_inputs<TP, TQ, PROBS>(a, static_cast<int>(bs), lane);
   uint64_t last_progress = global_ns();
   while (bs < static_cast<unsigned>(a.B) || bp < static_cast<unsigned>(a.B)) {
     bool progress = false;
@@ -797,8 +817,9 @@ __device__ void fu_finisher(const FusedArgs& a, FuShared& sh, int lane) {
       if (lane == 0) v = ld_relaxed_u32(a.cnt1 + bs);
       if (__shfl_sync(0xffffffffu, v, 0) == per_seq) {
         __threadfence();
-        finish_scan<TP, TQ, PROBS>(a, static_cast<int>(bs), lane);
+        finish_scan<TP, TQ, PROBS>(a, static_cast<int>(bs), lane, in);
         bs += G;
+        if (bs < static_cast<unsigned>(a.B)) in = scan_inputs<TP, TQ, PROBS>(a, static_cast<int>(bs), lane);
         progress = true;
       }
     }

@@ -327,27 +327,21 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   const int grid_cap = di.sms * per_sm;
   const int RB = PROBS ? K + 1 : 2 * K + 1;
   const long long rows = static_cast<long long>(B) * RB;
-  // sweep slices: ~48 KB units, but at least two units per CTA when the batch is small
+  // Sweep slices are whole ring stages (a row's last slice ends in its only
+  // partial stage), about four stages per unit; small batches use smaller
+  // units so that every CTA gets at least two.
   const int smax = max_slices(V);
-  const long long row_bytes = static_cast<long long>(V) * std::max(TP::esz, QE);
-  int S0 = std::max(1, ceil_div(row_bytes, 49152));
-  S0 = std::max(S0, static_cast<int>(std::min<long long>(smax, (2LL * grid_cap + rows - 1) / rows)));
-  S0 = std::min(S0, smax);
-  // Units are dealt round-robin and numbered sequence-major, so the last unit of
-  // sequence b lands on CTA (RB*S*(b+1) - 1) mod grid.  Choose S (or trim the
-  // grid) so that RB*S and the grid are coprime: completions -- and the scan
-  // tasks they create -- then rotate through all CTAs instead of a few.
-  auto gcd = [](long long x, long long y) { while (y) { const long long t = x % y; x = y; y = t; } return x; };
-  int S = S0, L = (ceil_div(V, S0) + 7) / 8 * 8, grid = grid_cap;
-  S = ceil_div(V, L);
-  bool found = false;
-  for (int s_try = S0; s_try <= std::min(smax, S0 + 8) && !found; ++s_try) {
-    const int l = (ceil_div(V, s_try) + 7) / 8 * 8;
-    const int se = ceil_div(V, l);
-    if (gcd(static_cast<long long>(RB) * se, grid_cap) == 1) { S = se; L = l; found = true; }
+  const int stage_elems = FU_STAGE / std::max(TP::esz, QE);
+  const int row_stages = ceil_div(V, stage_elems);
+  int per_unit = 4;
+  while (per_unit > 1 && rows * ceil_div(row_stages, per_unit) < 2LL * grid_cap) --per_unit;
+  int L = per_unit * stage_elems;
+  int S = ceil_div(V, L);
+  if (S > smax) {   // (only for tiny per-unit sizes) keep the partial count within the workspace bound
+    L = (ceil_div(V, smax) + 7) / 8 * 8;
+    S = ceil_div(V, L);
   }
-  for (int g = grid_cap; g > grid_cap - 32 && g > 1 && !found; --g)
-    if (gcd(static_cast<long long>(RB) * S, g) == 1) { grid = g; found = true; }
+  int grid = grid_cap;
   const long long U = rows * S;
   if (U >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "batch too large for one call");
   const int RE = (TP::esz == 2 && QE == 2) ? 4096 : 2048;   // residual stage: 16 KB of P+Q at most
