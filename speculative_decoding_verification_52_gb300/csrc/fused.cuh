@@ -787,7 +787,11 @@ __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& s
       const int prev = atomicAdd(&sh.unit_cnt[cur], 1);
       if (prev == FU_CW - 1) {
         sh.unit_cnt[cur] = 0;   // the slot's next item starts only after this warp releases it
-        __threadfence();
+        // The other warps' partial stores are ordered before their shared-memory
+        // increments (block fence); this warp observed those increments, and its
+        // block fence plus the gpu-scope release of the reduction carry all of
+        // them to whoever acquires the counter.
+        __threadfence_block();
         red_release_add_u32(d.kind == KIND_SWEEP ? a.cnt1 + d.b : a.cnt2 + d.b, 1u);
       }
       mbar_arrive(&sh.empty[cur]);
