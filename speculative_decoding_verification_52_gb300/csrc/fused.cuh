@@ -306,34 +306,28 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
   const int npart = a.S * FU_CW;
   const int x = in.x;
   const float u0 = in.u0;
-  // merge each row's S x 8 warp partials with the whole warp, four rows at a
-  // time with all their loads in flight; row r ends up in lane r & 31, slot r >> 5
+  // merge each row's S x 8 warp partials with the whole warp: lane i holds
+  // partial i of up to 16 rows at once (one round of loads for K <= 7 and
+  // S <= 4); row r ends up in lane r & 31, slot r >> 5
   float Ar[2] = {0.f, 0.f};
   double Sr[2] = {0.0, 0.0};
   int st[2] = {1, 1};
-  for (int r0 = 0; r0 < a.RB; r0 += 4) {
-    float2 pv[4][2];
+  for (int r0 = 0; r0 < a.RB; r0 += 16) {
+    float2 pv[16];
 #pragma unroll
-    for (int g = 0; g < 4; ++g)
+    for (int g = 0; g < 16; ++g) {
+      const int r = r0 + g;
+      pv[g] = (r < a.RB && lane < npart) ? __ldcg(a.part + (static_cast<long long>(b) * a.RB + r) * npart + lane)
+                                         : make_float2(kNegInf, 0.f);
+    }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = r0 + g, i = lane + 32 * h;
-        pv[g][h] = (r < a.RB && i < npart) ? __ldcg(a.part + (static_cast<long long>(b) * a.RB + r) * npart + i)
-                                            : make_float2(kNegInf, 0.f);
-      }
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < 16; ++g) {
       const int r = r0 + g;
       if (r >= a.RB) break;
       const float2* rowp = a.part + (static_cast<long long>(b) * a.RB + r) * npart;
-      float M = kNegInf;
-      bool poison = false;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (pv[g][h].x != pv[g][h].x) poison = true;
-        else M = fmaxf(M, pv[g][h].x);
-      }
-      for (int i = 64 + lane; i < npart; i += 32) {   // rows with more than 64 partials
+      bool poison = pv[g].x != pv[g].x;
+      float M = poison ? kNegInf : pv[g].x;
+      for (int i = 32 + lane; i < npart; i += 32) {   // rows with more than 32 partials
         const float2 p = __ldcg(rowp + i);
         if (p.x != p.x) poison = true;
         else M = fmaxf(M, p.x);
@@ -345,11 +339,9 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
       double acc = 0.0;
       if (!poison && M != kNegInf) {
         // fl(m*c) - fl(M*c) is exact in fp32 whenever the factor is not negligible
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (pv[g][h].x != kNegInf)
-            acc += static_cast<double>(pv[g][h].y) * static_cast<double>(exp2f(__fmul_rn(pv[g][h].x, a.c) - AM));
-        for (int i = 64 + lane; i < npart; i += 32) {
+        if (pv[g].x != kNegInf)
+          acc = static_cast<double>(pv[g].y) * static_cast<double>(exp2f(__fmul_rn(pv[g].x, a.c) - AM));
+        for (int i = 32 + lane; i < npart; i += 32) {
           const float2 p = __ldcg(rowp + i);
           if (p.x != kNegInf) acc += static_cast<double>(p.y) * static_cast<double>(exp2f(__fmul_rn(p.x, a.c) - AM));
         }
@@ -434,8 +426,8 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
     inf.pad = 0.f;
     a.info[b] = inf;
   }
+  // the warp's writes are ordered before lane 0's release by the warp barrier
   __syncwarp();
-  __threadfence();
   if (lane == 0) st_release_u32(a.ready + b, 1u);
 }
 
@@ -446,6 +438,10 @@ template <class TP, class TQ, bool PROBS>
 __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
   using QT = typename std::conditional<PROBS, F32T, TQ>::type;
   const int K = a.K, W = K + 1, V = a.V, NB = a.NB;
+  const int nbl = (NB + 31) / 32;               // blocks per lane (contiguous)
+  const int bl0 = min(NB, lane * nbl), bl1 = min(NB, bl0 + nbl);
+  float* brow = a.bsum + static_cast<long long>(b) * NB;
+  // the sequence's info and this lane's block sums in one round of loads
   SeqInfo inf;
   {
     const int* src = reinterpret_cast<const int*>(a.info + b);
@@ -453,15 +449,14 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) dst[i] = __ldcg(src + i);
   }
+  double lsum = 0.0;
+  for (int k = bl0; k < bl1; ++k) lsum += static_cast<double>(__ldcg(brow + k));
   if (inf.status != 0) return;   // outputs already written by the scan
   const unsigned char* prow = a.target + (static_cast<long long>(b) * W + inf.tstar) * V * TP::esz;
   const unsigned char* qrow =
       inf.tstar < K ? a.draft + (static_cast<long long>(b) * K + inf.tstar) * V * QT::esz : nullptr;
-  float* brow = a.bsum + static_cast<long long>(b) * NB;
   bool has_q = inf.tstar < K;
   const float c = a.c;
-  const int nbl = (NB + 31) / 32;               // blocks per lane (contiguous)
-  const int bl0 = min(NB, lane * nbl), bl1 = min(NB, bl0 + nbl);
 
   auto weights8 = [&](int e, float* w) {   // w of the 8 elements at e (e % 8 == 0)
     float zp[8], zq[8];
@@ -472,10 +467,12 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
       w[i] = resid_w(zp[i], has_q ? zq[i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q, PROBS);
   };
 
-  double lsum = 0.0, R = 0.0;
+  double R = 0.0;
   for (int pass = 0; pass < 2; ++pass) {
-    lsum = 0.0;
-    for (int k = bl0; k < bl1; ++k) lsum += static_cast<double>(__ldcg(brow + k));
+    if (pass > 0) {
+      lsum = 0.0;
+      for (int k = bl0; k < bl1; ++k) lsum += static_cast<double>(__ldcg(brow + k));
+    }
     R = lsum;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) R += __shfl_xor_sync(0xffffffffu, R, o);
