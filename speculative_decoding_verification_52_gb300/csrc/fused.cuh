@@ -3,7 +3,9 @@
 // exactness rule"; "Speculative decoding: draft, verify, repeat", steps 1-3;
 // "Speculative Decoding: from idea to SOTA", section 3).
 //
-// Work items (both kinds dealt round-robin to the CTAs, no atomics to claim):
+// Work items (both kinds dealt round-robin to the CTAs; a CTA claims its own
+// sweep units through a private cursor, and a CTA that has run out of its own
+// steals the last units of others, so slow CTAs do not delay the end):
 //   sweep unit    (sequence b, row r, slice j): softmax-normaliser partials
 //                 (max m, sum 2^(z*c - fl(m*c))) of one slice of one target or
 //                 draft row, numbered sequence-major so the batch is swept in
@@ -15,7 +17,7 @@
 //                 scan is done), ahead of its next sweep unit, so the stopping
 //                 rows are re-read while still in L2.
 // Roles inside a CTA:
-//   producer   (1 thread) streams work-item bytes into a 4-stage ring of 16 KB
+//   producer   (1 thread) streams work-item bytes into a 6-stage ring of 16 KB
 //              shared-memory stages with 1-D bulk async copies (cp.async.bulk,
 //              completion counted on an mbarrier per stage) and writes a small
 //              descriptor per stage.
@@ -48,7 +50,10 @@ constexpr int FU_CT = FU_CW * 32;
 constexpr int FU_THREADS = FU_CT + 64;            // + producer warp + finisher warp
 constexpr int FU_FIN_WARP = FU_CW + 1;
 constexpr int FU_STAGE = 16384;
-constexpr int FU_NSTAGE = 4;
+constexpr int FU_NSTAGE = 6;
+constexpr int FU_CTAS_PER_SM = 2;
+constexpr int FU_MAX_GRID = 1024;                 // cursor slots in the workspace
+constexpr int FU_CURSOR_STRIDE = 8;               // one 32-byte sector per cursor
 constexpr int FU_BLK = 256;                       // residual block (elements)
 
 enum : int { KIND_STOP = -1, KIND_SWEEP = 0, KIND_RESID = 1 };
@@ -88,6 +93,7 @@ struct FusedArgs {
   unsigned* cnt1;                // [B] sweep units completed
   unsigned* cnt2;                // [B] residual units completed
   unsigned* ready;               // [B] 1 once the accept scan has written SeqInfo
+  unsigned* cursor;              // [FU_MAX_GRID * FU_CURSOR_STRIDE] sweep units claimed per CTA
   SeqInfo* info;                 // [B]
   float* bsum;                   // [B * NB] residual block sums
   float2* part;                  // [U * FU_CW] sweep warp-partials
@@ -144,6 +150,14 @@ __device__ __forceinline__ float resid_w(float zp, float zq, float c, float nAP,
   if (!has_q) return wp;
   const float eq = probs ? zq : ex2_approx(__fmaf_rn(zq, c, nAQ));
   return fmaxf(0.f, __fmaf_rn(-eq, iSq, wp));
+}
+
+// error-free sum of two floats: (s, e) with s + e == a + b exactly (Knuth)
+__device__ __forceinline__ float2 two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return make_float2(s, e);
 }
 
 // 2^x for a double x <= 0 with ~1e-7 relative accuracy, without a double
@@ -306,53 +320,72 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
   const int npart = a.S * FU_CW;
   const int x = in.x;
   const float u0 = in.u0;
-  // merge each row's S x 8 warp partials with the whole warp: lane i holds
-  // partial i of up to 16 rows at once (one round of loads for K <= 7 and
-  // S <= 4); row r ends up in lane r & 31, slot r >> 5
+  // Merge each row's S x 8 warp partials with the whole warp, eight rows at a
+  // time with their reductions interleaved: lane i holds partial i of each
+  // row; the max is a shuffle tree, the rescaled sums are added in float-float
+  // (two-sum) arithmetic, which is exact to ~1e-14 without slow FP64 chains.
+  // Row r ends up in lane r & 31, slot r >> 5.
   float Ar[2] = {0.f, 0.f};
   double Sr[2] = {0.0, 0.0};
   int st[2] = {1, 1};
-  for (int r0 = 0; r0 < a.RB; r0 += 16) {
-    float2 pv[16];
+  for (int r0 = 0; r0 < a.RB; r0 += 8) {
+    float M[8], hi[8], lo[8];
+    bool bad[8];
 #pragma unroll
-    for (int g = 0; g < 16; ++g) {
+    for (int g = 0; g < 8; ++g) {
       const int r = r0 + g;
-      pv[g] = (r < a.RB && lane < npart) ? __ldcg(a.part + (static_cast<long long>(b) * a.RB + r) * npart + lane)
-                                         : make_float2(kNegInf, 0.f);
+      const float2* rowp = a.part + (static_cast<long long>(b) * a.RB + r) * npart;
+      M[g] = kNegInf;
+      bad[g] = false;
+      hi[g] = 0.f;
+      lo[g] = 0.f;
+      if (r < a.RB)
+        for (int i = lane; i < npart; i += 32) {
+          const float2 p = __ldcg(rowp + i);
+          if (p.x != p.x) bad[g] = true;
+          else M[g] = fmaxf(M[g], p.x);
+        }
     }
 #pragma unroll
-    for (int g = 0; g < 16; ++g) {
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int g = 0; g < 8; ++g) M[g] = fmaxf(M[g], __shfl_xor_sync(0xffffffffu, M[g], o));
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
       const int r = r0 + g;
-      if (r >= a.RB) break;
-      const float2* rowp = a.part + (static_cast<long long>(b) * a.RB + r) * npart;
-      bool poison = pv[g].x != pv[g].x;
-      float M = poison ? kNegInf : pv[g].x;
-      for (int i = 32 + lane; i < npart; i += 32) {   // rows with more than 32 partials
-        const float2 p = __ldcg(rowp + i);
-        if (p.x != p.x) poison = true;
-        else M = fmaxf(M, p.x);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      poison = __any_sync(0xffffffffu, poison);
-      const float AM = (M == kNegInf || poison) ? 0.f : __fmul_rn(M, a.c);
-      double acc = 0.0;
-      if (!poison && M != kNegInf) {
-        // fl(m*c) - fl(M*c) is exact in fp32 whenever the factor is not negligible
-        if (pv[g].x != kNegInf)
-          acc = static_cast<double>(pv[g].y) * static_cast<double>(exp2f(__fmul_rn(pv[g].x, a.c) - AM));
-        for (int i = 32 + lane; i < npart; i += 32) {
-          const float2 p = __ldcg(rowp + i);
-          if (p.x != kNegInf) acc += static_cast<double>(p.y) * static_cast<double>(exp2f(__fmul_rn(p.x, a.c) - AM));
+      bad[g] = __any_sync(0xffffffffu, bad[g]);
+      if (r < a.RB && !bad[g] && M[g] != kNegInf) {
+        const float AM = __fmul_rn(M[g], a.c);
+        const float2* rowp = a.part + (static_cast<long long>(b) * a.RB + r) * npart;
+        for (int i = lane; i < npart; i += 32) {
+          const float2 p = __ldcg(rowp + i);   // L2 hit (just loaded)
+          if (p.x == kNegInf) continue;
+          // fl(m*c) - fl(M*c) is exact in fp32 whenever the factor is not negligible
+          const float term = p.y * exp2f(__fmul_rn(p.x, a.c) - AM);
+          const float2 t = two_sum(hi[g], term);
+          hi[g] = t.x;
+          lo[g] += t.y;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       }
-      const int state = poison ? 2 : (M == kNegInf ? 1 : ((isfinite(acc) && acc > 0.0) ? 0 : 1));
-      if (lane == (r & 31)) {
-        Ar[r >> 5] = AM;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi[g], o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, lo[g], o);
+        const float2 t = two_sum(hi[g], h2);
+        hi[g] = t.x;
+        lo[g] = lo[g] + (l2 + t.y);
+      }
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const int r = r0 + g;
+      if (r < a.RB && lane == (r & 31)) {
+        const double acc = static_cast<double>(hi[g]) + static_cast<double>(lo[g]);
+        Ar[r >> 5] = (bad[g] || M[g] == kNegInf) ? 0.f : __fmul_rn(M[g], a.c);
         Sr[r >> 5] = acc;
-        st[r >> 5] = state;
+        st[r >> 5] = bad[g] ? 2 : (M[g] == kNegInf ? 1 : ((isfinite(acc) && acc > 0.0) ? 0 : 1));
       }
     }
   }
@@ -449,8 +482,14 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) dst[i] = __ldcg(src + i);
   }
+  constexpr int kRegBlocks = 16;   // block sums kept in registers per lane (V <= 131072)
+  float bv[kRegBlocks];
+#pragma unroll
+  for (int k = 0; k < kRegBlocks; ++k) bv[k] = (bl0 + k < bl1) ? __ldcg(brow + bl0 + k) : 0.f;
   double lsum = 0.0;
-  for (int k = bl0; k < bl1; ++k) lsum += static_cast<double>(__ldcg(brow + k));
+#pragma unroll
+  for (int k = 0; k < kRegBlocks; ++k) lsum += static_cast<double>(bv[k]);
+  for (int k = bl0 + kRegBlocks; k < bl1; ++k) lsum += static_cast<double>(__ldcg(brow + k));
   if (inf.status != 0) return;   // outputs already written by the scan
   const unsigned char* prow = a.target + (static_cast<long long>(b) * W + inf.tstar) * V * TP::esz;
   const unsigned char* qrow =
@@ -471,7 +510,12 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
   for (int pass = 0; pass < 2; ++pass) {
     if (pass > 0) {
       lsum = 0.0;
-      for (int k = bl0; k < bl1; ++k) lsum += static_cast<double>(__ldcg(brow + k));
+#pragma unroll
+      for (int k = 0; k < kRegBlocks; ++k) {
+        bv[k] = (bl0 + k < bl1) ? __ldcg(brow + bl0 + k) : 0.f;
+        lsum += static_cast<double>(bv[k]);
+      }
+      for (int k = bl0 + kRegBlocks; k < bl1; ++k) lsum += static_cast<double>(__ldcg(brow + k));
     }
     R = lsum;
 #pragma unroll
@@ -507,7 +551,17 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
   double jbase = 0.0, lastbase = 0.0;
   {
     double run = incl - lsum;
-    for (int k = bl0; k < bl1; ++k) {
+#pragma unroll
+    for (int k = 0; k < kRegBlocks; ++k) {
+      const double v = static_cast<double>(bv[k]);
+      if (v > 0.0) {
+        jlast = bl0 + k;
+        lastbase = run;
+        if (jb < 0 && run + v > target) { jb = bl0 + k; jbase = run; }
+      }
+      run += v;
+    }
+    for (int k = bl0 + kRegBlocks; k < bl1; ++k) {
       const double v = static_cast<double>(__ldcg(brow + k));
       if (v > 0.0) {
         jlast = k;
@@ -592,7 +646,6 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
   const unsigned RU = static_cast<unsigned>(a.B) * static_cast<unsigned>(a.Sr);
   const unsigned per_seq = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S);
   const int W = a.K + 1;
-  unsigned next_sweep = blockIdx.x;
   unsigned next_res = blockIdx.x;
   // readiness of the next residual unit's sequence: relaxed loads, issued one
   // unit ahead so their latency overlaps the copies
@@ -610,15 +663,41 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
     if (++stage == FU_NSTAGE) { stage = 0; phase ^= 1u; }
   };
 
+  // own sweep units are blockIdx + k * grid for k = 0, 1, ...; k is claimed on
+  // the CTA's cursor one unit ahead, so the claim's latency is hidden
+  const unsigned G = gridDim.x;
+  auto n_units = [&](unsigned c) { return a.U > c ? (a.U - c + G - 1) / G : 0u; };
+  const unsigned n_own = n_units(blockIdx.x);
+  unsigned own_k = atomicAdd(a.cursor + blockIdx.x * FU_CURSOR_STRIDE, 1u);
+  unsigned victim = 0, steal_fails = 0;
+  bool stealing = true;
   bool ok = true;
   while (ok) {
     long long rid = -1, uid = -1;
     if (next_res < RU && res_ready) {
       rid = next_res;
-      next_res += gridDim.x;
-    } else if (next_sweep < a.U) {
-      uid = next_sweep;
-      next_sweep += gridDim.x;
+      next_res += G;
+    } else if (own_k < n_own) {
+      uid = blockIdx.x + static_cast<long long>(own_k) * G;
+      own_k = atomicAdd(a.cursor + blockIdx.x * FU_CURSOR_STRIDE, 1u);
+    } else if (stealing) {
+      // take the next unclaimed unit of another CTA (victims in a fixed order)
+      victim = (victim + 1) % G;
+      const unsigned v = (blockIdx.x + victim * 97u) % G;
+      if (v != blockIdx.x) {
+        const unsigned k = atomicAdd(a.cursor + v * FU_CURSOR_STRIDE, 1u);
+        if (k < n_units(v)) {
+          uid = v + static_cast<long long>(k) * G;
+          steal_fails = 0;
+        } else if (++steal_fails >= 16) {
+          stealing = false;
+        }
+      }
+      if (victim + 1 >= G) stealing = false;
+      if (uid < 0) {
+        res_ready = next_res < RU ? ld_relaxed_u32(a.ready + next_res / a.Sr) : 0u;
+        continue;
+      }
     } else if (next_res < RU) {
       // sweep done: wait for the next residual unit's sequence
       const uint64_t t0 = global_ns();
@@ -632,7 +711,7 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
         break;
       }
       rid = next_res;
-      next_res += gridDim.x;
+      next_res += G;
     } else {
       break;
     }
@@ -854,7 +933,7 @@ __device__ void fu_finisher(const FusedArgs& a, FuShared& sh, int lane) {
 constexpr size_t fu_smem_bytes() { return FU_NSTAGE * FU_STAGE + sizeof(FuShared) + 128; }
 
 template <class TP, class TQ, bool PROBS>
-__global__ void __launch_bounds__(FU_THREADS, 3) fused_sample_kernel(const FusedArgs a) {
+__global__ void __launch_bounds__(FU_THREADS, FU_CTAS_PER_SM) fused_sample_kernel(const FusedArgs a) {
   extern __shared__ __align__(128) unsigned char fu_smem[];
   unsigned char* ring = fu_smem;
   FuShared& sh = *reinterpret_cast<FuShared*>(fu_smem + FU_NSTAGE * FU_STAGE);

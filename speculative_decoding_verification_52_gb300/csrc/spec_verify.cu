@@ -282,15 +282,16 @@ int finish_max_cluster(int dev) {
 }
 
 // Workspace of the fused sampling kernel:
-//   [FuCtl | cnt1[B] | cnt2[B] | ready[B]]              zeroed per call
+//   [FuCtl | cnt1[B] | cnt2[B] | ready[B] | cursor[1024 x 8]]   zeroed per call
 //   [info[B] | bsum[B * ceil(V/256)] | part[rows * S * 8]]
 struct FusedLayout {
-  size_t zero_bytes, info_off, bsum_off, part_off, total;
+  size_t cursor_off, zero_bytes, info_off, bsum_off, part_off, total;
 };
 FusedLayout fused_layout(int B, int K, int V) {
   FusedLayout l{};
   const size_t nb = static_cast<size_t>((V + FU_BLK - 1) / FU_BLK);
-  l.zero_bytes = align_up(32 + 12u * static_cast<size_t>(B), 16);
+  l.cursor_off = align_up(32 + 12u * static_cast<size_t>(B), 32);
+  l.zero_bytes = l.cursor_off + sizeof(unsigned) * FU_MAX_GRID * FU_CURSOR_STRIDE;
   l.info_off = l.zero_bytes;
   l.bsum_off = align_up(l.info_off + sizeof(SeqInfo) * static_cast<size_t>(B), 16);
   l.part_off = align_up(l.bsum_off + sizeof(float) * static_cast<size_t>(B) * nb, 16);
@@ -324,7 +325,7 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   constexpr int QE = PROBS ? 4 : TQ::esz;
   const int per_sm = fused_per_sm<TP, TQ, PROBS>(dev);
   if (per_sm <= 0) return fail(SPEC_ERR_CUDA, "fused kernel setup failed: %s", cudaGetErrorString(cudaGetLastError()));
-  const int grid_cap = di.sms * per_sm;
+  const int grid_cap = std::min(FU_MAX_GRID, di.sms * per_sm);
   const int RB = PROBS ? K + 1 : 2 * K + 1;
   const long long rows = static_cast<long long>(B) * RB;
   // Sweep slices are whole ring stages (a row's last slice ends in its only
@@ -371,6 +372,7 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   a.cnt1 = reinterpret_cast<unsigned*>(w + 32);
   a.cnt2 = a.cnt1 + B;
   a.ready = a.cnt2 + B;
+  a.cursor = reinterpret_cast<unsigned*>(w + lay.cursor_off);
   a.info = reinterpret_cast<SeqInfo*>(w + lay.info_off);
   a.bsum = reinterpret_cast<float*>(w + lay.bsum_off);
   a.part = reinterpret_cast<float2*>(w + lay.part_off);

@@ -24,17 +24,18 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_workspace_sizes(L):
-    # control block (32 B) + per-sequence counters and readiness flags, per-sequence
-    # info (32 B), residual block sums (ceil(V/256) floats per sequence), and
-    # per-warp slice partials (rows x ceil(V/2048) x 8 warps x 8 B)
+    # control block (32 B) + per-sequence counters and readiness flags + 1024
+    # per-CTA claim cursors (32 B each), per-sequence info (32 B), residual
+    # block sums (ceil(V/256) floats per sequence), and per-warp slice partials
+    # (rows x ceil(V/2048) x 8 warps x 8 B)
     def al(x, a):
         return (x + a - 1) // a * a
     B_, K_, V_ = 256, 5, 128256
-    zero = al(32 + 12 * B_, 16)
+    zero = al(32 + 12 * B_, 32) + 1024 * 32
     bsum = al(zero + 32 * B_, 16)
     part = al(bsum + 4 * B_ * (-(-V_ // 256)), 16)
     assert L.spec_workspace_bytes(B_, K_, V_) == al(part + B_ * (2 * K_ + 1) * 63 * 8 * 8, 256)
-    assert L.spec_workspace_bytes(1, 0, 8) == 256
+    assert L.spec_workspace_bytes(1, 0, 8) == al(al(al(al(32 + 12, 32) + 1024 * 32 + 32, 16) + 4, 16) + 64, 256)
     assert L.spec_tree_workspace_bytes(128, 64, 128256) == 128 * 64 * 63 * 8
     for bad in [(-1, 4, 10), (1, -1, 10), (1, 32, 10), (1, 4, 0)]:
         assert L.spec_workspace_bytes(*bad) == 0
