@@ -50,8 +50,8 @@ constexpr int FU_CT = FU_CW * 32;
 constexpr int FU_THREADS = FU_CT + 64;            // + producer warp + finisher warp
 constexpr int FU_FIN_WARP = FU_CW + 1;
 constexpr int FU_STAGE = 16384;
-constexpr int FU_NSTAGE = 6;
-constexpr int FU_CTAS_PER_SM = 2;
+constexpr int FU_NSTAGE = 4;
+constexpr int FU_CTAS_PER_SM = 3;
 constexpr int FU_MAX_GRID = 1024;                 // cursor slots in the workspace
 constexpr int FU_CURSOR_STRIDE = 8;               // one 32-byte sector per cursor
 constexpr int FU_BLK = 256;                       // residual block (elements)
