@@ -155,10 +155,12 @@ spec_status_t spec_debug_residual(const void *target_logits, spec_dtype_t target
                                   size_t workspace_bytes, void *stream);
 
 /* Timing hooks for benchmarks: while enabled, each verify call records CUDA
- * events around its vocabulary-sweep kernel and around its finishing kernel on
- * the call's stream (at most max_calls calls are recorded).  spec_profile_end
- * synchronises on the recorded events and returns the summed milliseconds of
- * each part and the number of recorded calls.  Not thread-safe. */
+ * events on the call's stream around its kernels (at most max_calls calls are
+ * recorded).  spec_profile_end synchronises on the recorded events and returns
+ * the summed milliseconds of each part and the number of recorded calls.  For
+ * two-kernel paths the parts are the vocabulary sweep and the finishing
+ * kernel; the fused sampling path is one kernel, timed as the first part (the
+ * second part is then ~0).  Not thread-safe. */
 spec_status_t spec_profile_begin(int max_calls);
 spec_status_t spec_profile_end(float *sweep_ms, float *finish_ms, int *calls);
 

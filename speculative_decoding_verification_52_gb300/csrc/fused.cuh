@@ -17,7 +17,7 @@
 //                 scan is done), ahead of its next sweep unit, so the stopping
 //                 rows are re-read while still in L2.
 // Roles inside a CTA:
-//   producer   (1 thread) streams work-item bytes into a 6-stage ring of 16 KB
+//   producer   (1 thread) streams work-item bytes into a ring of FU_NSTAGE 16 KB
 //              shared-memory stages with 1-D bulk async copies (cp.async.bulk,
 //              completion counted on an mbarrier per stage) and writes a small
 //              descriptor per stage.
