@@ -108,6 +108,35 @@ spec_status_t spec_verify_sample(const void *target_logits, spec_dtype_t target_
                                  int32_t *out_tokens, int32_t *num_accepted, void *workspace,
                                  size_t workspace_bytes, void *stream);
 
+/* spec_verify_sample without a caller workspace; it allocates nothing.  The
+ * method on the pages has no counterpart: this is an interface variant for
+ * callers that cannot hand over device scratch at call time, e.g. a plain C
+ * decode loop with no device allocator of its own, or one that must not call
+ * cudaMalloc/cudaFree between steps because those synchronise the device.
+ *
+ * Arguments, semantics, outputs and errors are those of spec_verify_sample.
+ * Scratch comes from a fixed 16 MiB (16777216-byte) device array inside the
+ * library.  A batch whose spec_workspace_bytes(B, K, V) exceeds that returns
+ * SPEC_ERR_UNSUPPORTED (spec_last_error() gives both sizes); B=256, K=5,
+ * V=128256 needs 11.9 MB and fits.
+ *
+ * The first call on each device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress, which may load the
+ * library's device code; make that first call before any stream capture.
+ * Later calls on that device reuse the address.
+ *
+ * The array is shared by every call on a device: calls that may overlap on the
+ * GPU (different streams, different host threads) race on it and must be
+ * serialised by the caller.  Each call clears the part that must start at zero
+ * (the kernel's control block and counters) on its own stream before its
+ * kernel runs. */
+spec_status_t spec_verify_sample_noalloc(const void *target_logits, spec_dtype_t target_dtype,
+                                         const void *draft, spec_dtype_t draft_dtype,
+                                         spec_draft_kind_t draft_kind,
+                                         const int32_t *draft_tokens, const float *uniforms,
+                                         float temperature, int B, int K, int V,
+                                         int32_t *out_tokens, int32_t *num_accepted, void *stream);
+
 /* Greedy verification ("The exactness rule", greedy case): g_t = argmax of
  * target row t (lowest index on ties, raw logits, no temperature); accept x_t
  * while g_t == x_t; emit g_t at the first mismatch, or g_K when all K match.

@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
             L.spec_tree_workspace_bytes.restype = Z
             L.spec_verify_sample.argtypes = [P, I, P, I, I, P, P, F, I, I, I, P, P, P, Z, P]
             L.spec_verify_sample.restype = I
+            L.spec_verify_sample_noalloc.argtypes = [P, I, P, I, I, P, P, F, I, I, I, P, P, P]
+            L.spec_verify_sample_noalloc.restype = I
             L.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, Z, P]
             L.spec_verify_greedy.restype = I
             L.spec_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P, P, Z, P]
@@ -160,6 +162,27 @@ def spec_verify_sample(target_logits, draft, draft_tokens, uniforms, temperature
                                   _ptr(out_tokens), _ptr(num_accepted), _ptr(workspace_buf),
                                   workspace_buf.numel(), _stream(stream))
     _check("spec_verify_sample", st)
+    return out_tokens, num_accepted
+
+
+def spec_verify_sample_noalloc(target_logits, draft, draft_tokens, uniforms, temperature, *,
+                               draft_kind: str = "logits", out_tokens=None, num_accepted=None, stream=None):
+    """spec_verify_sample with the library's fixed scratch instead of a
+    workspace.  Pass out_tokens / num_accepted to keep the call free of any
+    allocation (otherwise they are allocated here)."""
+    _dev(target_logits, "target_logits")
+    B, W, V = target_logits.shape
+    K = W - 1
+    kind = SPEC_DRAFT_PROBS if draft_kind == "probs" else SPEC_DRAFT_LOGITS
+    for t, n in ((draft, "draft"), (draft_tokens, "draft_tokens"), (uniforms, "uniforms")):
+        if t is not None:
+            _dev(t, n)
+    ddt = _dtype_code(draft) if draft is not None else SPEC_F32
+    out_tokens, num_accepted = _outputs(B, W, target_logits.device, out_tokens, num_accepted)
+    st = lib().spec_verify_sample_noalloc(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), ddt, kind,
+                                          _ptr(draft_tokens), _ptr(uniforms), float(temperature), B, K, V,
+                                          _ptr(out_tokens), _ptr(num_accepted), _stream(stream))
+    _check("spec_verify_sample_noalloc", st)
     return out_tokens, num_accepted
 
 

@@ -520,6 +520,42 @@ spec_status_t sample_entry(const void* target, spec_dtype_t tdt, const void* dra
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// fixed scratch for spec_verify_sample_noalloc
+// ---------------------------------------------------------------------------
+// A file-scope device array stands in for the caller's workspace, so that call
+// allocates nothing.  It holds kNoallocScratchBytes (16 MiB: the B=256, K=5,
+// V=128256 batch needs 11.9 MB).  Every call on a device uses the same array:
+// calls that may overlap on the GPU (other streams, other host threads) race
+// on it.  The part of it that must start at zero (the fused kernel's control
+// block and counters) is cleared on the call's stream by every call, exactly as
+// for a caller-supplied workspace; the rest is written before it is read.
+constexpr size_t kNoallocScratchBytes = static_cast<size_t>(16) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+namespace {
+
+// Device address of the array in the current device's context.  Resolved once
+// per device, on the first call made with that device current; later calls
+// only read the cached pointer.
+spec_status_t noalloc_scratch(int dev, void** out) {
+  static void* ptr[kMaxDevices] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 0 || dev >= kMaxDevices) return fail(SPEC_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed scratch)");
+    if (!p) return fail(SPEC_ERR_CUDA, "cudaGetSymbolAddress returned a NULL scratch address");
+    ptr[dev] = p;
+  }
+  *out = ptr[dev];
+  return SPEC_OK;
+}
+
+}  // namespace
+
 // ===========================================================================
 // exported C ABI
 // ===========================================================================
@@ -545,6 +581,35 @@ spec_status_t spec_verify_sample(const void* target_logits, spec_dtype_t target_
   try {
     return sample_entry(target_logits, target_dtype, draft, draft_dtype, draft_kind, draft_tokens, uniforms,
                         temperature, B, K, V, out_tokens, num_accepted, workspace, workspace_bytes, -1, -1, nullptr,
+                        nullptr, stream);
+  } catch (...) {
+    return fail(SPEC_ERR_CUDA, "unexpected host exception");
+  }
+}
+
+spec_status_t spec_verify_sample_noalloc(const void* target_logits, spec_dtype_t target_dtype, const void* draft,
+                                         spec_dtype_t draft_dtype, spec_draft_kind_t draft_kind,
+                                         const int32_t* draft_tokens, const float* uniforms, float temperature, int B,
+                                         int K, int V, int32_t* out_tokens, int32_t* num_accepted, void* stream) {
+  try {
+    const size_t need = spec_workspace_bytes(B, K, V);
+    if (B == 0 || need == 0)   // empty batch or bad sizes: argument checks only, nothing launched
+      return sample_entry(target_logits, target_dtype, draft, draft_dtype, draft_kind, draft_tokens, uniforms,
+                          temperature, B, K, V, out_tokens, num_accepted, nullptr, 0, -1, -1, nullptr, nullptr,
+                          stream);
+    if (need > kNoallocScratchBytes)
+      return fail(SPEC_ERR_UNSUPPORTED,
+                  "B=%d K=%d V=%d needs %zu scratch bytes; spec_verify_sample_noalloc holds %zu "
+                  "(use spec_verify_sample with a caller workspace)",
+                  B, K, V, need, kNoallocScratchBytes);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    void* ws = nullptr;
+    spec_status_t s = noalloc_scratch(dev, &ws);
+    if (s != SPEC_OK) return s;
+    return sample_entry(target_logits, target_dtype, draft, draft_dtype, draft_kind, draft_tokens, uniforms,
+                        temperature, B, K, V, out_tokens, num_accepted, ws, kNoallocScratchBytes, -1, -1, nullptr,
                         nullptr, stream);
   } catch (...) {
     return fail(SPEC_ERR_CUDA, "unexpected host exception");
