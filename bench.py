@@ -1,23 +1,30 @@
 #!/usr/bin/env python
-"""Benchmark of batched draft-token verification (sampling mode) on GB300.
+"""Benchmark of batched draft-token verification on GB300.
 
-One step = one spec_verify_sample call over the B=256, V=128256, K=5, bf16,
-T=0.7 workload (target logits [256,6,128256], draft logits [256,5,128256]):
-the vocabulary sweep over all 2816 rows plus the per-sequence accept scan and
-replacement/bonus draw, all inside one persistent kernel launch (after a
-small memset of the workspace's control block).  Inputs are generated once (seeded, synthetic), copied
-to HBM, and the timed region covers exactly --steps calls bracketed by a
-barrier and a device synchronisation, timed with CUDA events.  The inputs
-(722 MB) are larger than the L2 cache, so no flush is needed between steps.
+Default workload ("sample"): one step = one spec_verify_sample call over the
+B=256, V=128256, K=5, bf16, T=0.7 batch (target logits [256,6,128256], draft
+logits [256,5,128256]): the vocabulary sweep over all 2816 rows plus the
+per-sequence accept scan and replacement/bonus draw, all inside one persistent
+kernel launch (after a small memset of the workspace's control block).
 
-Metric: verified draft positions per second (B*K per call), whole job.
-Also reported: the fused kernel's achieved HBM bandwidth against the measured
-copy peak (roofline; algorithmic bytes = every row once plus one re-read
-target row per sequence), an end-to-end figure with host<->device copies inside
-the timed region, the SM clocks seen during the run, and the double-precision
-CPU oracle timed on a bounded sample on this host.
+Other workloads (--workload):
+  greedy  spec_verify_greedy at the same shape (target rows only, T = 0)
+  tree    spec_verify_tree_greedy, B=128, N=64 nodes (BFS [4,3,2,1] truncated),
+          V=128256, bf16
+
+Inputs are generated once (seeded, synthetic), copied to HBM, and the timed
+region covers exactly --steps calls bracketed by a barrier and a device
+synchronisation, timed with CUDA events.  Every workload's inputs are larger
+than the L2 cache (129 MB), so no flush is needed between steps.
+
+Reported: the metric (verified draft positions/s; tree: candidate nodes/s),
+the dominant kernel's achieved HBM bandwidth against the measured copy peak
+(roofline), an end-to-end figure with host<->device copies inside the timed
+region, the SM clocks seen during the run, and the double-precision CPU
+oracle timed on a bounded sample on this host.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload sample|greedy|tree]
 """
 from __future__ import annotations
 
@@ -37,20 +44,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 B, V, K, T = 256, 128256, 5, 0.7
-WORKLOAD = "spec-verify sampling B=256 V=128256 K=5 bf16 T=0.7 (target+draft logits, accept scan, residual/bonus draw)"
+TREE_B, TREE_N = 128, 64
 METRIC = "verified draft positions/s"
 UNIT = "positions/s"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fused_sample_kernel_b256_v128256_k5_bf16.md")
-KERNEL = "fused_sample_kernel<bf16 target, bf16 draft logits>"
 
 
 def sweep_bytes(b=B, k=K, v=V, elem=2):
-    """Algorithmic bytes of one sweep launch: every target and draft row once."""
+    """Bytes of one pass over every target and draft row."""
     return b * (2 * k + 1) * v * elem
 
 
 def metric_bytes(b=B, k=K, v=V, elem=2):
-    """Bytes of one verify call: one pass over all rows + one stopping target row per sequence."""
+    """Algorithmic bytes of one sampling call: one pass over all rows + one
+    stopping target row per sequence."""
     return (b * (k + 1) * v + b * k * v + b * v) * elem
 
 
@@ -64,12 +70,12 @@ def source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """dram read+write bytes per fused-kernel launch from the committed ncu
-    summary, only if it was taken on the current kernel sources."""
+def profiled_traffic(summary: str):
+    """dram read+write bytes per launch of the dominant kernel from a committed
+    ncu summary, only if it was taken on the current kernel sources."""
     try:
         kv = {}
-        with open(PROFILE_SUMMARY) as f:
+        with open(os.path.join(ROOT, "profiles", summary)) as f:
             for line in f:
                 if ":" in line:
                     k_, v_ = line.split(":", 1)
@@ -137,23 +143,25 @@ class ClockSampler:
                 "power_w_max": max((float(r[4]) for r in rows if r[4].replace(".", "").isdigit()), default=None)}
 
 
-def oracle_positions_per_s(batch, budget_s: float, min_seqs: int = 4):
-    """The oracle, as it stands, over sequences of `batch` until ~budget_s of CPU work."""
-    import numpy as np
+# ---------------------------------------------------------------------------
+# multi-rank host logic (replicas over sequences, weak scaling)
+# ---------------------------------------------------------------------------
+def rank_sequences(rank: int, per_rank: int) -> list[int]:
+    """Sequence ids of one rank: every rank verifies its own batch, disjoint
+    from the others' (sequences are independent; nothing is exchanged)."""
+    return list(range(rank * per_rank, (rank + 1) * per_rank))
 
-    import oracle
-    oracle.build()
-    done, t_used = 0, 0.0
-    while t_used < budget_s or done < min_seqs:   # cycles over the batch's sequences, 4 per call
-        s0 = done % batch.B
-        sl = slice(s0, min(batch.B, s0 + 4))
-        t0 = time.perf_counter()
-        oracle.verify_sample(batch.target[sl], batch.dtype, batch.draft[sl], batch.dtype, False,
-                             np.ascontiguousarray(batch.draft_tokens[sl]), np.ascontiguousarray(batch.uniforms[sl]),
-                             batch.T)
-        t_used += time.perf_counter() - t0
-        done += sl.stop - sl.start
-    return done * batch.K / t_used, done, t_used
+
+def max_over_ranks(values, ws: int, device=None):
+    """Element-wise max of per-rank timings (the slowest rank sets the job's time)."""
+    values = [float(v) for v in values]
+    if ws <= 1:
+        return values
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
 
 
 def dist_setup():
@@ -170,66 +178,258 @@ def dist_setup():
     return ws, rank, local
 
 
-def run_reference(args, ws, rank):
-    """The oracle arm: the double-precision CPU oracle on this host's cores,
-    each step a bounded sample (4 sequences) of the same workload."""
-    if rank != 0:
-        return
-    from speculative_decoding_verification_52_gb300 import inputs as gen
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+class Workload:
+    """One benchmarked call: its batch, the metric's units per step, the
+    dominant kernel and its algorithmic bytes, and the oracle's CPU leg."""
+    name = ""
+    metric = METRIC
+    unit = UNIT
+    summary = ""
+    kernel = ""
+    per_rank = B
+    launches_per_step = 1
+
+    def describe(self) -> dict:
+        raise NotImplementedError
+
+    def batch(self, seqs):
+        raise NotImplementedError
+
+    def units(self, batch) -> int:
+        raise NotImplementedError
+
+    def algorithmic_bytes(self, batch) -> int:
+        raise NotImplementedError
+
+    def oracle_call(self, batch, sl):
+        raise NotImplementedError
+
+    def oracle_chunk(self) -> int:
+        return 4
+
+    def device_setup(self, batch, dev):
+        """Returns (host inputs, device inputs they are copied to, step(),
+        device outputs)."""
+        raise NotImplementedError
+
+
+def _bf16_host(x):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+
+def _pinned(x):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+
+
+class SampleWorkload(Workload):
+    name = "sample"
+    summary = "fused_sample_kernel_b256_v128256_k5_bf16.md"
+    kernel = "fused_sample_kernel<bf16 target, bf16 draft logits>"
+
+    def describe(self):
+        return {"workload": "spec-verify sampling B=256 V=128256 K=5 bf16 T=0.7 (target+draft logits, accept scan, "
+                            "residual/bonus draw)", "B": B, "V": V, "K": K, "temperature": T,
+                "input_bytes": sweep_bytes(), "metric_bytes_per_step": metric_bytes(),
+                "l2": "inputs (722 MB) larger than L2; no flush"}
+
+    def batch(self, seqs):
+        from speculative_decoding_verification_52_gb300 import inputs as gen
+        return gen.config_headline(seqs=seqs)
+
+    def units(self, batch):
+        return batch.B * batch.K
+
+    def algorithmic_bytes(self, batch):
+        return metric_bytes(batch.B, batch.K, batch.V)
+
+    def oracle_call(self, batch, sl):
+        import numpy as np
+
+        import oracle
+        oracle.verify_sample(batch.target[sl], batch.dtype, batch.draft[sl], batch.dtype, False,
+                             np.ascontiguousarray(batch.draft_tokens[sl]), np.ascontiguousarray(batch.uniforms[sl]),
+                             batch.T)
+
+    def device_setup(self, batch, dev):
+        import torch
+
+        import speculative_decoding_verification_52_gb300 as sv
+        hs = [_bf16_host(batch.target), _bf16_host(batch.draft), _pinned(batch.draft_tokens),
+              _pinned(batch.uniforms)]
+        ds = [h.to(dev) for h in hs]
+        out = torch.empty((batch.B, batch.K + 1), dtype=torch.int32, device=dev)
+        nacc = torch.empty((batch.B,), dtype=torch.int32, device=dev)
+        wsb = sv.workspace(sv.spec_workspace_bytes(batch.B, batch.K, batch.V), dev)
+        stream = torch.cuda.current_stream()
+
+        def step():
+            sv.spec_verify_sample(ds[0], ds[1], ds[2], ds[3], batch.T, out_tokens=out, num_accepted=nacc,
+                                  workspace_buf=wsb, stream=stream)
+        return hs, ds, step, [out, nacc]
+
+
+class GreedyWorkload(Workload):
+    name = "greedy"
+    summary = "sweep_argmax_greedy_b256_v128256_k5_bf16.md"
+    kernel = "sweep_tma_kernel<bf16, argmax>"
+    launches_per_step = 2
+
+    def describe(self):
+        return {"workload": "spec-verify greedy B=256 V=128256 K=5 bf16 (target-row argmax, chain match)",
+                "B": B, "V": V, "K": K, "temperature": 0.0, "input_bytes": B * (K + 1) * V * 2,
+                "l2": "inputs (394 MB) larger than L2; no flush"}
+
+    def batch(self, seqs):
+        from speculative_decoding_verification_52_gb300 import inputs as gen
+        return gen.config_headline(seqs=seqs)
+
+    def units(self, batch):
+        return batch.B * batch.K
+
+    def algorithmic_bytes(self, batch):
+        return batch.B * (batch.K + 1) * batch.V * 2
+
+    def oracle_call(self, batch, sl):
+        import numpy as np
+
+        import oracle
+        oracle.verify_greedy(batch.target[sl], batch.dtype, np.ascontiguousarray(batch.draft_tokens[sl]))
+
+    def device_setup(self, batch, dev):
+        import torch
+
+        import speculative_decoding_verification_52_gb300 as sv
+        hs = [_bf16_host(batch.target), _pinned(batch.draft_tokens)]
+        ds = [h.to(dev) for h in hs]
+        out = torch.empty((batch.B, batch.K + 1), dtype=torch.int32, device=dev)
+        nacc = torch.empty((batch.B,), dtype=torch.int32, device=dev)
+        wsb = sv.workspace(sv.spec_workspace_bytes(batch.B, batch.K, batch.V), dev)
+        stream = torch.cuda.current_stream()
+
+        def step():
+            sv.spec_verify_greedy(ds[0], ds[1], out_tokens=out, num_accepted=nacc, workspace_buf=wsb, stream=stream)
+        return hs, ds, step, [out, nacc]
+
+
+class TreeWorkload(Workload):
+    name = "tree"
+    metric = "verified candidate tree nodes/s"
+    unit = "nodes/s"
+    summary = "sweep_argmax_tree_b128_n64_v128256_bf16.md"
+    kernel = "sweep_tma_kernel<bf16, argmax>"
+    per_rank = TREE_B
+    launches_per_step = 2
+
+    def describe(self):
+        return {"workload": "spec-verify tree greedy B=128 N=64 (BFS [4,3,2,1] truncated) V=128256 bf16",
+                "B": TREE_B, "N": TREE_N, "V": V, "input_bytes": TREE_B * TREE_N * V * 2,
+                "l2": "inputs (2.10 GB) larger than L2; no flush"}
+
+    def batch(self, seqs):
+        from speculative_decoding_verification_52_gb300 import inputs as gen
+        return gen.config_tree(seqs=seqs)
+
+    def units(self, batch):
+        return batch.B * (batch.N - 1)
+
+    def algorithmic_bytes(self, batch):
+        return batch.B * batch.N * batch.V * 2
+
+    def oracle_chunk(self):
+        return 1
+
+    def oracle_call(self, batch, sl):
+        import numpy as np
+
+        import oracle
+        oracle.verify_tree_greedy(batch.target[sl], batch.dtype, batch.parents,
+                                  np.ascontiguousarray(batch.node_tokens[sl]), batch.max_depth)
+
+    def device_setup(self, batch, dev):
+        import numpy as np
+        import torch
+
+        import speculative_decoding_verification_52_gb300 as sv
+        hs = [_bf16_host(batch.target), _pinned(batch.node_tokens)]
+        ds = [h.to(dev) for h in hs]
+        parents = torch.from_numpy(np.ascontiguousarray(batch.parents, dtype=np.int32)).to(dev)
+        W = batch.max_depth + 1
+        out = torch.empty((batch.B, W), dtype=torch.int32, device=dev)
+        nacc = torch.empty((batch.B,), dtype=torch.int32, device=dev)
+        path = torch.empty((batch.B, W), dtype=torch.int32, device=dev)
+        wsb = sv.workspace(sv.spec_tree_workspace_bytes(batch.B, batch.N, batch.V), dev)
+        stream = torch.cuda.current_stream()
+
+        def step():
+            sv.spec_verify_tree_greedy(ds[0], parents, ds[1], batch.max_depth, out_tokens=out, num_accepted=nacc,
+                                       out_path=path, workspace_buf=wsb, stream=stream)
+        return hs, ds, step, [out, nacc, path]
+
+
+WORKLOADS = {w.name: w for w in (SampleWorkload(), GreedyWorkload(), TreeWorkload())}
+
+
+def oracle_rate(wl: Workload, batch, budget_s: float, min_seqs: int):
+    """The oracle, as it stands, over the batch's sequences (cycled, a few per
+    call) until about budget_s of CPU work; returns (units/s, sequences, seconds)."""
     import oracle
     oracle.build()
-    per_step = 4
-    batch = gen.config_headline(seqs=list(range(per_step)))
+    per_seq_units = wl.units(batch) / batch.B
+    done, t_used = 0, 0.0
+    while t_used < budget_s or done < min_seqs:
+        s0 = done % batch.B
+        sl = slice(s0, min(batch.B, s0 + wl.oracle_chunk()))
+        t0 = time.perf_counter()
+        wl.oracle_call(batch, sl)
+        t_used += time.perf_counter() - t0
+        done += sl.stop - sl.start
+    return done * per_seq_units / t_used, done, t_used
+
+
+def run_reference(args, wl: Workload, ws, rank):
+    """The oracle arm: the double-precision CPU oracle on this host's cores,
+    each step a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    per_step = wl.oracle_chunk()
+    batch = wl.batch(list(range(per_step)))
     for _ in range(max(0, args.warmup)):
-        oracle_positions_per_s(batch, 0.0, min_seqs=per_step)
+        oracle_rate(wl, batch, 0.0, per_step)
     t = 0.0
     for _ in range(args.steps):
-        _, done, dt = oracle_positions_per_s(batch, 0.0, min_seqs=per_step)
+        _, _, dt = oracle_rate(wl, batch, 0.0, per_step)
         t += dt
-    value = args.steps * per_step * K / t
-    sample = f"{per_step} of the 256 sequences per step"
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+    value = args.steps * wl.units(batch) / t
+    sample = f"{per_step} of the {wl.per_rank} sequences per step"
+    line = {"impl": "reference", "metric": wl.metric, "value": value, "unit": wl.unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "B": B, "V": V, "K": K, "temperature": T},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "data": "synthetic", "config": wl.describe(),
+            "cpu_baseline": {"value": value, "unit": wl.unit, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, ws, rank, local):
-    import numpy as np
+def run_ours(args, wl: Workload, ws, rank, local):
     import torch
 
     import speculative_decoding_verification_52_gb300 as sv
-    from speculative_decoding_verification_52_gb300 import inputs as gen
 
     assert torch.cuda.is_available(), "bench.py needs a CUDA device"
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sv.lib()
 
-    # weak scaling: every rank verifies its own batch of 256 sequences
-    seqs = list(range(rank * B, (rank + 1) * B))
-    batch = gen.config_headline(seqs=seqs)
-
-    def bf(x, pin=False):
-        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
-        return t.pin_memory() if pin else t
-
-    h_target, h_draft = bf(batch.target, True), bf(batch.draft, True)
-    h_tok = torch.from_numpy(batch.draft_tokens).pin_memory()
-    h_uni = torch.from_numpy(batch.uniforms).pin_memory()
-    target, draft = h_target.to(dev), h_draft.to(dev)
-    tok, uni = h_tok.to(dev), h_uni.to(dev)
-    out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
-    nacc = torch.empty((B,), dtype=torch.int32, device=dev)
-    wsb = sv.workspace(sv.spec_workspace_bytes(B, K, V), dev)
+    batch = wl.batch(rank_sequences(rank, wl.per_rank))
+    hs, ds, step, douts = wl.device_setup(batch, dev)
     stream = torch.cuda.current_stream()
-
-    def step():
-        sv.spec_verify_sample(target, draft, tok, uni, T, out_tokens=out, num_accepted=nacc, workspace_buf=wsb,
-                              stream=stream)
 
     def barrier():
         if ws > 1:
@@ -253,22 +453,21 @@ def run_ours(args, ws, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    kern_ms, _, ncalls = sv.spec_profile_end()   # fused kernel time (events around its launch)
+    # events around the kernels of each call: part 1 = the sweep (the whole
+    # fused kernel, for sampling), part 2 = the finishing kernel (none when fused)
+    kern_ms, fin_ms, ncalls = sv.spec_profile_end()
     ms = e0.elapsed_time(e1) / args.steps
 
     # end to end through the public API: pinned host inputs -> HBM -> verify -> host outputs
-    h_out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
-    h_nacc = torch.empty((B,), dtype=torch.int32).pin_memory()
+    houts = [torch.empty(d.shape, dtype=d.dtype).pin_memory() for d in douts]
     e2e_steps = max(3, min(args.steps, 50))
 
     def e2e_step():
-        target.copy_(h_target, non_blocking=True)
-        draft.copy_(h_draft, non_blocking=True)
-        tok.copy_(h_tok, non_blocking=True)
-        uni.copy_(h_uni, non_blocking=True)
+        for h, d in zip(hs, ds):
+            d.copy_(h, non_blocking=True)
         step()
-        h_out.copy_(out, non_blocking=True)
-        h_nacc.copy_(nacc, non_blocking=True)
+        for h, d in zip(houts, douts):
+            h.copy_(d, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -284,44 +483,40 @@ def run_ours(args, ws, rank, local):
     e2e_ms = f0.elapsed_time(f1) / e2e_steps
     clk = clocks.stop()
 
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, e2e_ms, kern_ms / max(1, ncalls)], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms, kern_avg_ms = t.tolist()
-    else:
-        kern_avg_ms = kern_ms / max(1, ncalls)
-
+    n = max(1, ncalls)
+    ms, e2e_ms, kern_avg_ms, fin_avg_ms = max_over_ranks([ms, e2e_ms, kern_ms / n, fin_ms / n], ws, dev)
     if rank != 0:
         return
     peaks, src = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", 6800.0))
-    achieved = metric_bytes() / (kern_avg_ms * 1e-3) / 1e9
-    value = ws * B * K / (ms * 1e-3)
+    alg = wl.algorithmic_bytes(batch)
+    achieved = alg / (kern_avg_ms * 1e-3) / 1e9
+    units = wl.units(batch)
     cpu = None
     if ws == 1:
-        cpu_rate, done, cpu_t = oracle_positions_per_s(batch, budget_s=args.cpu_budget)
-        cpu = {"value": cpu_rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{done} sequence verifications (the 256 sequences of the same workload, cycled), "
+        cpu_rate, done, cpu_t = oracle_rate(wl, batch, args.cpu_budget, 4)
+        cpu = {"value": cpu_rate, "unit": wl.unit, "cores": 1, "kind": "oracle",
+               "sample": f"{done} sequence verifications (the {batch.B} sequences of the same workload, cycled), "
                          f"single-threaded double-precision C oracle, {cpu_t:.1f} s"}
-    h2d = sum(x.numel() * x.element_size() for x in (h_target, h_draft, h_tok, h_uni))
-    d2h = h_out.numel() * 4 + h_nacc.numel() * 4
+    cfg = wl.describe()
+    cfg["parallelism"] = f"replicas over sequences x{ws}"
+    cfg["metric_GBps"] = alg / (ms * 1e-3) / 1e9
+    cfg["metric_frac_of_8TBps"] = alg / (ms * 1e-3) / 8e12
+    roof = {"bound": "hbm", "kernel": wl.kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "peak_source": f"{src} hbm_gbs (burst copy)",
+            "traffic": profiled_traffic(wl.summary), "algorithmic_bytes": alg, "avg_launch_ms": kern_avg_ms}
+    if wl.launches_per_step > 1:
+        roof["finish_avg_ms"] = fin_avg_ms
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "V": V, "K": K, "temperature": T,
-                   "input_bytes": sweep_bytes(), "metric_bytes_per_step": metric_bytes(),
-                   "metric_GBps": metric_bytes() / (ms * 1e-3) / 1e9,
-                   "metric_frac_of_8TBps": metric_bytes() / (ms * 1e-3) / 8e12,
-                   "l2": "inputs (722 MB) larger than L2; no flush", "parallelism": f"replicas over sequences x{ws}"},
-        "roofline": {"bound": "hbm", "kernel": KERNEL, "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "peak_source": f"{src} hbm_gbs (burst copy)",
-                     "traffic": profiled_traffic(), "algorithmic_bytes": metric_bytes(),
-                     "avg_launch_ms": kern_avg_ms},
-        "e2e": {"value": ws * B * K / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,   # one fused kernel per step (plus one cudaMemsetAsync of the control block)
+        "metric": wl.metric, "value": ws * units / (ms * 1e-3), "unit": wl.unit, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": cfg, "roofline": roof,
+        "e2e": {"value": ws * units / (e2e_ms * 1e-3), "unit": wl.unit,
+                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in hs),
+                "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in houts), "ms_per_step": e2e_ms},
+        # our kernels per step: the fused kernel (sampling; plus one cudaMemsetAsync
+        # of its control block), or sweep + finish (greedy, tree)
+        "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
@@ -334,15 +529,17 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="sample")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    wl = WORKLOADS[args.workload]
     ws, rank, local = dist_setup()
     if args.impl == "reference":
-        run_reference(args, ws, rank)
+        run_reference(args, wl, ws, rank)
     else:
-        run_ours(args, ws, rank, local)
+        run_ours(args, wl, ws, rank, local)
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()

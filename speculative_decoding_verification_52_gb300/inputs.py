@@ -45,9 +45,14 @@ SIGMA_B256_V128K = 0.445
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float values to bfloat16 (nearest, ties to even); return uint16 bits."""
     f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
-    b = f.view(np.uint32).astype(np.uint64)
-    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
-    return b.astype(np.uint16)
+    b = f.view(np.uint32)
+    # b + 0x7FFF + lsb stays below 2^32 for every finite or infinite value
+    # (the largest, 0xFF800000, gains at most 0x8000)
+    r = (b >> 16) & 1
+    r += 0x7FFF
+    r += b
+    r >>= 16
+    return r.astype(np.uint16)
 
 
 def bf16_bits_to_f64(h: np.ndarray) -> np.ndarray:
