@@ -8,9 +8,13 @@ per-sequence accept scan and replacement/bonus draw, all inside one persistent
 kernel launch (after a small memset of the workspace's control block).
 
 Other workloads (--workload):
-  greedy  spec_verify_greedy at the same shape (target rows only, T = 0)
+  greedy  spec_verify_greedy, B=256, V=128256, K=5, bf16; draft token t is the
+          target row's argmax with probability 0.8
   tree    spec_verify_tree_greedy, B=128, N=64 nodes (BFS [4,3,2,1] truncated),
-          V=128256, bf16
+          V=128256, bf16; node tokens copy the parent's argmax with probability 0.7
+Both read only the rows the greedy rules need (rows up to the first mismatch;
+accepted tree nodes), one persistent kernel per call; their algorithmic bytes
+are those rows, counted from the generator's own copy draws.
 
 Inputs are generated once (seeded, synthetic), copied to HBM, and the timed
 region covers exactly --steps calls bracketed by a barrier and a device
@@ -275,26 +279,34 @@ class SampleWorkload(Workload):
         return hs, ds, step, [out, nacc]
 
 
+def leading_true(flags):
+    """Per row, the number of leading True entries."""
+    import numpy as np
+    f = np.asarray(flags, dtype=bool)
+    return np.where(f.all(axis=1), f.shape[1], np.argmin(f, axis=1))
+
+
 class GreedyWorkload(Workload):
     name = "greedy"
-    summary = "sweep_argmax_greedy_b256_v128256_k5_bf16.md"
-    kernel = "sweep_tma_kernel<bf16, argmax>"
-    launches_per_step = 2
+    summary = "tree_greedy_kernel_chain_b256_v128256_k5_bf16.md"
+    kernel = "tree_greedy_kernel<bf16> (chain mode)"
 
     def describe(self):
-        return {"workload": "spec-verify greedy B=256 V=128256 K=5 bf16 (target-row argmax, chain match)",
-                "B": B, "V": V, "K": K, "temperature": 0.0, "input_bytes": B * (K + 1) * V * 2,
-                "l2": "inputs (394 MB) larger than L2; no flush"}
+        return {"workload": "spec-verify greedy B=256 V=128256 K=5 bf16, draft = target argmax w.p. 0.8 "
+                            "(rows up to the first mismatch)", "B": B, "V": V, "K": K, "temperature": 0.0,
+                "input_bytes": B * (K + 1) * V * 2, "l2": "inputs (394 MB) larger than L2; no flush"}
 
     def batch(self, seqs):
         from speculative_decoding_verification_52_gb300 import inputs as gen
-        return gen.config_headline(seqs=seqs)
+        return gen.config_greedy(seqs=seqs)
 
     def units(self, batch):
         return batch.B * batch.K
 
     def algorithmic_bytes(self, batch):
-        return batch.B * (batch.K + 1) * batch.V * 2
+        # rows 0..n per sequence, n = accepted drafts = leading copied positions
+        rows = int((leading_true(batch.meta["copied"]) + 1).sum())
+        return rows * batch.V * 2
 
     def oracle_call(self, batch, sl):
         import numpy as np
@@ -322,10 +334,9 @@ class TreeWorkload(Workload):
     name = "tree"
     metric = "verified candidate tree nodes/s"
     unit = "nodes/s"
-    summary = "sweep_argmax_tree_b128_n64_v128256_bf16.md"
-    kernel = "sweep_tma_kernel<bf16, argmax>"
+    summary = "tree_greedy_kernel_b128_n64_v128256_bf16.md"
+    kernel = "tree_greedy_kernel<bf16>"
     per_rank = TREE_B
-    launches_per_step = 2
 
     def describe(self):
         return {"workload": "spec-verify tree greedy B=128 N=64 (BFS [4,3,2,1] truncated) V=128256 bf16",
@@ -340,7 +351,14 @@ class TreeWorkload(Workload):
         return batch.B * (batch.N - 1)
 
     def algorithmic_bytes(self, batch):
-        return batch.B * batch.N * batch.V * 2
+        # accepted nodes' rows: a node is accepted iff every node on its path
+        # from the root drew a copy of its parent's argmax
+        import numpy as np
+        acc = np.zeros((batch.B, batch.N), dtype=bool)
+        acc[:, 0] = True
+        for j in range(1, batch.N):
+            acc[:, j] = acc[:, batch.parents[j]] & batch.copied[:, j]
+        return int(acc.sum()) * batch.V * 2
 
     def oracle_chunk(self):
         return 1
@@ -500,6 +518,7 @@ def run_ours(args, wl: Workload, ws, rank, local):
                          f"single-threaded double-precision C oracle, {cpu_t:.1f} s"}
     cfg = wl.describe()
     cfg["parallelism"] = f"replicas over sequences x{ws}"
+    cfg["algorithmic_bytes_per_step"] = alg
     cfg["metric_GBps"] = alg / (ms * 1e-3) / 1e9
     cfg["metric_frac_of_8TBps"] = alg / (ms * 1e-3) / 8e12
     roof = {"bound": "hbm", "kernel": wl.kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -514,8 +533,8 @@ def run_ours(args, wl: Workload, ws, rank, local):
         "e2e": {"value": ws * units / (e2e_ms * 1e-3), "unit": wl.unit,
                 "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in hs),
                 "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in houts), "ms_per_step": e2e_ms},
-        # our kernels per step: the fused kernel (sampling; plus one cudaMemsetAsync
-        # of its control block), or sweep + finish (greedy, tree)
+        # our kernels per step: one persistent kernel (plus one cudaMemsetAsync of
+        # its control block)
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,

@@ -24,6 +24,7 @@
 #include "fused.cuh"
 #include "spec_verify.h"
 #include "sweep.cuh"
+#include "tree.cuh"
 
 namespace {
 
@@ -194,9 +195,21 @@ bool dtype_ok(spec_dtype_t d) { return d == SPEC_F32 || d == SPEC_BF16; }
 // greedy chain
 // ---------------------------------------------------------------------------
 template <class T>
+spec_status_t run_tree_pruned(const DevInfo& di, int dev, const void* target, const int32_t* parents,
+                              const int32_t* node_tokens, int B, int N, int V, int max_depth, int32_t* out,
+                              int32_t* nacc, int32_t* path, void* ws, cudaStream_t st, bool chain);
+
+template <class T>
 spec_status_t run_greedy(const DevInfo& di, int dev, const void* target, const int32_t* tokens, int B, int K, int V,
                          int32_t* out, int32_t* nacc, void* ws, cudaStream_t st) {
   const bool vec = aligned16(target) && (static_cast<long long>(V) * T::esz) % 16 == 0;
+  if (vec) {
+    // the chain as a tree of K+1 nodes: rows after the first mismatch are not read
+    const spec_status_t s = run_tree_pruned<T>(di, dev, target, nullptr, tokens, B, K + 1, V, K, out, nacc, nullptr,
+                                               ws, st, true);
+    if (s != SPEC_ERR_UNSUPPORTED) return s;
+  }
+  // full sweep of the K+1 target rows, then one warp per sequence
   const long long rows = static_cast<long long>(B) * (K + 1);
   float2* part = reinterpret_cast<float2*>(ws);
   prof_mark(0, st);
@@ -468,6 +481,97 @@ spec_status_t dispatch_sample(const DevInfo& di, int dev, const void* target, sp
 #undef SV_RUN
 }
 
+// ---------------------------------------------------------------------------
+// greedy tree, pruned (one persistent kernel)
+// ---------------------------------------------------------------------------
+// Workspace of the pruned tree kernel:
+//   [TrCtl (128 B) | cnt[B*N] | fifo[B*(N-1)*S]]   zeroed per call
+//   [part[B*N*S*8]]
+struct TreeLayout {
+  size_t fifo_off, zero_bytes, part_off, total;
+};
+TreeLayout tree_layout(int B, int N, int S) {
+  TreeLayout l{};
+  const size_t nodes = static_cast<size_t>(B) * static_cast<size_t>(N);
+  const size_t qcap = static_cast<size_t>(B) * static_cast<size_t>(N - 1) * static_cast<size_t>(S);
+  l.fifo_off = align_up(128 + sizeof(unsigned) * nodes, 128);
+  l.zero_bytes = l.fifo_off + sizeof(unsigned) * qcap;
+  l.part_off = align_up(l.zero_bytes, 256);
+  l.total = align_up(l.part_off + nodes * static_cast<size_t>(S) * TR_CW * sizeof(float2), 256);
+  return l;
+}
+// most slices a row can have: a unit is at least one 16 KB stage of f32
+int tree_max_slices(int V) { return std::max(1, ceil_div(V, TR_STAGE / 4)); }
+
+template <class T>
+int tree_per_sm(int dev) {
+  static int per_sm[kMaxDevices];
+  auto kern = tree_greedy_kernel<T>;
+  once_per_device(dev, [&] {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(tr_smem_bytes())) !=
+        cudaSuccess)
+      return false;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, TR_THREADS, tr_smem_bytes()) != cudaSuccess)
+      return false;
+    per_sm[dev] = std::max(1, n);
+    return true;
+  });
+  return per_sm[dev];
+}
+
+// Returns SPEC_ERR_UNSUPPORTED (nothing launched) when the batch needs more
+// sequences per finisher than the kernel holds; the caller then takes the
+// full-sweep path.
+template <class T>
+spec_status_t run_tree_pruned(const DevInfo& di, int dev, const void* target, const int32_t* parents,
+                              const int32_t* node_tokens, int B, int N, int V, int max_depth, int32_t* out,
+                              int32_t* nacc, int32_t* path, void* ws, cudaStream_t st, bool chain) {
+  const int per_sm = tree_per_sm<T>(dev);
+  if (per_sm <= 0) return fail(SPEC_ERR_CUDA, "tree kernel setup failed: %s", cudaGetErrorString(cudaGetLastError()));
+  const int grid = di.sms * per_sm;
+  if (N > TR_MAX_N || B > TR_MAX_SEQ * grid) return SPEC_ERR_UNSUPPORTED;
+  // units of up to 4 stages; smaller when the roots alone would not give every CTA two units
+  const int stage_elems = TR_STAGE / T::esz;
+  const int row_stages = ceil_div(V, stage_elems);
+  int per_unit = 4;
+  while (per_unit > 1 && static_cast<long long>(B) * ceil_div(row_stages, per_unit) < 2LL * grid) --per_unit;
+  const int L = per_unit * stage_elems;
+  const int S = ceil_div(V, L);
+  if (static_cast<long long>(B) * N * S >= (1LL << 31)) return SPEC_ERR_UNSUPPORTED;
+  const TreeLayout lay = tree_layout(B, N, S);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  TreeArgs a{};
+  a.target = static_cast<const unsigned char*>(target);
+  a.parents = parents;
+  a.node_tokens = node_tokens;
+  a.B = B;
+  a.N = N;
+  a.V = V;
+  a.S = S;
+  a.L = L;
+  a.max_depth = max_depth;
+  a.chain = chain ? 1 : 0;
+  a.qcap = static_cast<unsigned>(static_cast<long long>(B) * (N - 1) * S);
+  a.ctl = reinterpret_cast<TrCtl*>(w);
+  a.cnt = reinterpret_cast<unsigned*>(w + 128);
+  a.fifo = reinterpret_cast<unsigned*>(w + lay.fifo_off);
+  a.part = reinterpret_cast<float2*>(w + lay.part_off);
+  a.out_tokens = out;
+  a.num_accepted = nacc;
+  a.out_path = path;
+  a.timeout_ns = kWaitNs;
+  cudaError_t e = cudaMemsetAsync(ws, 0, lay.zero_bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "tree workspace reset");
+  prof_mark(0, st);
+  tree_greedy_kernel<T><<<grid, TR_THREADS, tr_smem_bytes(), st>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "tree kernel launch");
+  prof_mark(1, st);
+  prof_mark(2, st);
+  return SPEC_OK;
+}
+
 spec_status_t check_chain_args(const void* target, spec_dtype_t tdt, const int32_t* tokens, int B, int K, int V,
                                int32_t* out, int32_t* nacc) {
   if (B < 0) return fail(SPEC_ERR_INVALID_ARG, "B=%d must be >= 0", B);
@@ -565,13 +669,15 @@ size_t spec_workspace_bytes(int B, int K, int V) {
   if (B < 0 || K < 0 || K > SPEC_MAX_K || V < 1) return 0;
   const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(2 * K + 1);
   const size_t plain = align_up(rows * static_cast<size_t>(max_slices(V)) * sizeof(float2), 256);
-  return std::max(plain, fused_layout(B, K, V).total);
+  const size_t chain = tree_layout(B, K + 1, tree_max_slices(V)).total;   // greedy rule, pruned kernel
+  return std::max(std::max(plain, chain), fused_layout(B, K, V).total);
 }
 
 size_t spec_tree_workspace_bytes(int B, int N, int V) {
   if (B < 0 || N < 1 || N > SPEC_MAX_TREE_NODES || V < 1) return 0;
   const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(N);
-  return align_up(rows * static_cast<size_t>(max_slices(V)) * sizeof(float2), 256);
+  const size_t full = align_up(rows * static_cast<size_t>(max_slices(V)) * sizeof(float2), 256);
+  return std::max(full, tree_layout(B, N, tree_max_slices(V)).total);
 }
 
 spec_status_t spec_verify_sample(const void* target_logits, spec_dtype_t target_dtype, const void* draft,
@@ -678,6 +784,16 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t ta
     const long long rows = static_cast<long long>(B) * N;
     const int esz = esz_of(target_dtype);
     const bool vec = aligned16(target_logits) && (static_cast<long long>(V) * esz) % 16 == 0;
+    if (vec) {
+      // pruned: only accepted nodes' rows are swept
+      s = target_dtype == SPEC_BF16
+              ? run_tree_pruned<BF16T>(di, dev, target_logits, parents, node_tokens, B, N, V, max_depth, out_tokens,
+                                       num_accepted, out_path, workspace, st, false)
+              : run_tree_pruned<F32T>(di, dev, target_logits, parents, node_tokens, B, N, V, max_depth, out_tokens,
+                                      num_accepted, out_path, workspace, st, false);
+      if (s != SPEC_ERR_UNSUPPORTED) return s;
+    }
+    // full sweep of every node row, then one CTA per sequence resolves the tree
     float2* part = reinterpret_cast<float2*>(workspace);
     prof_mark(0, st);
     int S = 0;

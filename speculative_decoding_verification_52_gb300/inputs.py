@@ -122,6 +122,7 @@ class TreeBatch:
     node_tokens: np.ndarray    # [B, N] int32 (node 0's entry is ignored)
     max_depth: int
     name: str = ""
+    copied: np.ndarray | None = None   # [B, N] bool: the generator set the token to the parent's argmax
 
 
 def _uniforms(rng: np.random.Generator, K: int) -> np.ndarray:
@@ -226,6 +227,31 @@ def config_controlled(B: int, K: int, V: int = 151936, copy_prob: float = 0.8,
                       meta=dict(copied=copied, copy_prob=copy_prob, seed=seed, seqs=seqs))
 
 
+def config_greedy(B: int = 256, V: int = 128256, K: int = 5, match_prob: float = 0.8,
+                  seed: int = 52_600, seqs=None, dtype: str = BF16) -> ChainBatch:
+    """Greedy chain verification with controlled agreement: target rows ~ N(0,1);
+    the draft token at position t is the argmax of target row t with
+    probability ``match_prob``, else uniform in [0, V) (``meta["copied"]``
+    records which).  No draft rows or uniforms: the greedy rule reads neither."""
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    n = len(seqs)
+    tgt = np.empty((n, K + 1, V), dtype=np.uint16 if dtype == BF16 else np.float32)
+    tok = np.empty((n, K), dtype=np.int32)
+    copied = np.zeros((n, K), dtype=bool)
+    for i, b in enumerate(seqs):
+        rng = _rng(seed, b)
+        tgt[i] = _store(rng.standard_normal((K + 1, V)), dtype)
+        for t in range(K):
+            if rng.random() < match_prob:
+                tok[i, t] = int(np.argmax(as_f64(tgt[i, t], dtype)))
+                copied[i, t] = True
+            else:
+                tok[i, t] = int(rng.integers(0, V))
+    return ChainBatch(n, K, V, 0.0, dtype, tgt, np.zeros((n, K, 0), dtype=tgt.dtype), False, tok,
+                      np.zeros((n, K + 1, 2), dtype=np.float32), name=f"greedy_B{B}_K{K}",
+                      meta=dict(copied=copied, match_prob=match_prob, seed=seed, seqs=seqs))
+
+
 def bfs_tree(branching, max_nodes=None) -> np.ndarray:
     """Parent array of a static tree in breadth-first order: the root, then
     ``branching[0]`` children of the root, then ``branching[1]`` children of
@@ -265,6 +291,7 @@ def config_tree(B: int = 128, V: int = 128256, branching=(4, 3, 2, 1), N: int = 
     n = len(seqs)
     tgt = np.empty((n, N, V), dtype=np.uint16 if dtype == BF16 else np.float32)
     tok = np.empty((n, N), dtype=np.int32)
+    copied = np.zeros((n, N), dtype=bool)
     for i, b in enumerate(seqs):
         rng = _rng(seed, b)
         tgt[i] = _store(rng.standard_normal((N, V)), dtype)
@@ -273,13 +300,14 @@ def config_tree(B: int = 128, V: int = 128256, branching=(4, 3, 2, 1), N: int = 
         for j in range(1, N):
             if rng.random() < match_prob:
                 tok[i, j] = int(np.argmax(rows[parents[j]]))
+                copied[i, j] = True
             else:
                 tok[i, j] = int(rng.integers(0, V))
-    return TreeBatch(n, N, V, dtype, tgt, parents, tok, depth, name=f"tree_B{B}_N{N}")
+    return TreeBatch(n, N, V, dtype, tgt, parents, tok, depth, name=f"tree_B{B}_N{N}", copied=copied)
 
 
 __all__ = [
-    "F32", "BF16", "ChainBatch", "TreeBatch", "SIGMA_B256_V128K",
+    "F32", "BF16", "ChainBatch", "TreeBatch", "SIGMA_B256_V128K", "config_greedy",
     "f32_to_bf16_bits", "bf16_bits_to_f64", "as_f64", "gaussian_chain",
     "config_tiny", "config_zipf", "config_headline", "config_controlled",
     "config_tree", "bfs_tree", "tree_depths",

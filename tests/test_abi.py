@@ -34,9 +34,15 @@ def test_workspace_sizes(L):
     zero = al(32 + 12 * B_, 32) + 1024 * 32
     bsum = al(zero + 32 * B_, 16)
     part = al(bsum + 4 * B_ * (-(-V_ // 256)), 16)
-    assert L.spec_workspace_bytes(B_, K_, V_) == al(part + B_ * (2 * K_ + 1) * 63 * 8 * 8, 256)
-    assert L.spec_workspace_bytes(1, 0, 8) == al(al(al(al(32 + 12, 32) + 1024 * 32 + 32, 16) + 4, 16) + 64, 256)
-    assert L.spec_tree_workspace_bytes(128, 64, 128256) == 128 * 64 * 63 * 8
+    fused = al(part + B_ * (2 * K_ + 1) * 63 * 8 * 8, 256)
+    assert L.spec_workspace_bytes(B_, K_, V_) == fused   # larger than the greedy chain's pruned layout here
+    fused1 = al(al(al(al(32 + 12, 32) + 1024 * 32 + 32, 16) + 4, 16) + 64, 256)
+    assert L.spec_workspace_bytes(1, 0, 8) == max(fused1, al(256 + 64, 256))
+    # tree: max(full sweep partials, pruned-kernel layout with at most ceil(V/4096) slices)
+    nodes, smax = 128 * 64, -(-128256 // 4096)
+    fifo = al(128 + 4 * nodes, 128)
+    pruned = al(al(fifo + 4 * 128 * 63 * smax, 256) + nodes * smax * 8 * 8, 256)
+    assert L.spec_tree_workspace_bytes(128, 64, 128256) == max(128 * 64 * 63 * 8, pruned)
     for bad in [(-1, 4, 10), (1, -1, 10), (1, 32, 10), (1, 4, 0)]:
         assert L.spec_workspace_bytes(*bad) == 0
     assert L.spec_tree_workspace_bytes(1, 0, 10) == 0

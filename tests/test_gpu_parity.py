@@ -322,6 +322,81 @@ def test_tree_bad_topology_and_nan(orc):
     assert rn.tolist() == [3, 3, -1]
 
 
+@pytest.mark.parametrize("dt,V", [("bf16", 32768), ("f32", 4000)])
+def test_greedy_controlled_agreement(orc, dt, V):
+    """Greedy rule on drafts that copy the target argmax w.p. 0.8: long accepted
+    prefixes, so rows well past position 0 are needed (and rows after the first
+    mismatch are not)."""
+    b = gen.config_greedy(B=96, V=V, K=7, dtype=dt)
+    ro, rn = orc.verify_greedy(b.target, b.dtype, b.draft_tokens)
+    out, n = sv.spec_verify_greedy(gu.dev_tensor(b.target, b.dtype), gu.i32(b.draft_tokens))
+    np.testing.assert_array_equal(n.cpu().numpy(), rn)
+    np.testing.assert_array_equal(out.cpu().numpy(), ro)
+    assert rn.mean() > 2
+
+
+def _tree_case(rng, parents, B, V, dtype, match=0.7):
+    N = len(parents)
+    z = rng.standard_normal((B, N, V))
+    rows = gen.f32_to_bf16_bits(z) if dtype == "bf16" else z.astype(np.float32)
+    g = np.argmax(gen.as_f64(rows, dtype), axis=-1)
+    tok = np.where(rng.random((B, N)) < match, g[:, np.maximum(parents, 0)],
+                   rng.integers(0, V, size=(B, N))).astype(np.int32)
+    return rows, tok
+
+
+def _tree_check(orc, rows, dtype, parents, tok, depth):
+    ro, rn, rp = orc.verify_tree_greedy(rows, dtype, parents, tok, depth)
+    out, n, path = sv.spec_verify_tree_greedy(gu.dev_tensor(rows, dtype), gu.i32(parents), gu.i32(tok), depth)
+    np.testing.assert_array_equal(n.cpu().numpy(), rn)
+    np.testing.assert_array_equal(out.cpu().numpy(), ro)
+    np.testing.assert_array_equal(path.cpu().numpy(), rp)
+    return rn
+
+
+@pytest.mark.parametrize("shape", ["chain48", "wide1024", "deep_bushy"])
+def test_tree_pruned_shapes(orc, shape):
+    """Dependency chains much deeper than the headline tree, and node counts up
+    to the 1024-node limit (every node bit in use)."""
+    rng = np.random.default_rng({"chain48": 1, "wide1024": 2, "deep_bushy": 3}[shape])
+    if shape == "chain48":
+        parents = gen.bfs_tree([1] * 47)            # 48 nodes in one chain
+        rows, tok = _tree_case(rng, parents, 6, 4096, "bf16", match=0.97)
+    elif shape == "wide1024":
+        parents = gen.bfs_tree([32, 31], max_nodes=1024)
+        rows, tok = _tree_case(rng, parents, 3, 2048, "bf16", match=0.9)
+    else:
+        parents = gen.bfs_tree([3, 2, 2, 2, 2, 2, 2], max_nodes=300)
+        rows, tok = _tree_case(rng, parents, 5, 1000, "f32", match=0.8)
+    depth = int(gen.tree_depths(parents).max())
+    rn = _tree_check(orc, rows, "bf16" if shape != "deep_bushy" else "f32", parents, tok, depth)
+    assert rn.max() >= 2
+
+
+@pytest.mark.parametrize("B", [600, 2000])
+def test_tree_many_sequences(orc, B):
+    """More sequences than CTAs (several per finisher), and beyond the pruned
+    kernel's per-finisher limit (the full-sweep path)."""
+    rng = np.random.default_rng(B)
+    parents = gen.bfs_tree([3, 2, 2], max_nodes=20)
+    rows, tok = _tree_case(rng, parents, B, 256, "bf16")
+    _tree_check(orc, rows, "bf16", parents, tok, int(gen.tree_depths(parents).max()))
+
+
+def test_tree_nan_outside_accepted_nodes_is_ignored(orc):
+    """Only accepted nodes' rows are read: a NaN in a rejected node's row does
+    not invalidate the sequence; one in an accepted node's row does."""
+    rng = np.random.default_rng(7)
+    parents = gen.bfs_tree([2, 2])                  # 7 nodes: 0 | 1 2 | 3 4 5 6
+    rows, tok = _tree_case(rng, parents, 4, 512, "f32", match=1.0)
+    tok[:, 2] = (tok[:, 1] + 1) % 512                # node 2 (and 5, 6) rejected
+    rows[0, 2, 17] = np.nan                          # rejected: ignored
+    rows[1, 5, 3] = np.nan                           # rejected descendant: ignored
+    rows[2, 3, 9] = np.nan                           # accepted leaf: invalid
+    rn = _tree_check(orc, rows, "f32", parents, tok, 2)
+    assert rn[0] >= 0 and rn[1] >= 0 and rn[2] == -1
+
+
 def test_calls_finish_without_hitting_wait_bounds():
     """Every wait in the kernels is bounded (1 s); a call that silently ran into
     a bound would still be correct but slow.  The headline-sized call must take
@@ -333,12 +408,18 @@ def test_calls_finish_without_hitting_wait_bounds():
     sv.spec_verify_sample(tgt, dft, tok, uni, b.T)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    t = gen.config_tree(seqs=list(range(16)), V=32768)
+    ttgt, tpar, ttok = gu.dev_tensor(t.target, t.dtype), gu.i32(t.parents), gu.i32(t.node_tokens)
+    sv.spec_verify_tree_greedy(ttgt, tpar, ttok, t.max_depth)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
     for _ in range(5):
         _, n = sv.spec_verify_sample(tgt, dft, tok, uni, b.T)
         sv.spec_verify_greedy(tgt, tok)
+        _, tn, _ = sv.spec_verify_tree_greedy(ttgt, tpar, ttok, t.max_depth)
     torch.cuda.synchronize()
     assert time.perf_counter() - t0 < 0.5
-    assert (n.cpu().numpy() >= 0).all()
+    assert (n.cpu().numpy() >= 0).all() and (tn.cpu().numpy() >= 0).all()
 
 
 def test_non_default_stream(orc):

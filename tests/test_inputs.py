@@ -64,3 +64,30 @@ def test_tree_topology_and_tokens():
     rows = gen.as_f64(t.target, t.dtype)
     match = [t.node_tokens[b, j] == np.argmax(rows[b, t.parents[j]]) for b in range(4) for j in range(1, 64)]
     assert 0.55 < np.mean(match) < 0.85
+
+
+def test_greedy_copy_flags_predict_the_oracle(orc):
+    """The greedy workload's copy draws fix how many drafts the greedy rule
+    accepts (leading copied positions), which the benchmark uses to count the
+    rows the rule needs."""
+    b = gen.config_greedy(B=24, V=2048, K=6)
+    out, n = orc.verify_greedy(b.target, b.dtype, b.draft_tokens)
+    f = b.meta["copied"]
+    lead = np.where(f.all(axis=1), f.shape[1], np.argmin(f, axis=1))
+    np.testing.assert_array_equal(n, lead)
+    assert 0 < n.mean() < b.K
+
+
+def test_tree_copy_flags_predict_the_oracle(orc):
+    """Tree workload: a node is accepted iff every node on its root path copied
+    its parent's argmax; the oracle's chosen depth is the deepest such node."""
+    t = gen.config_tree(seqs=list(range(12)), V=1024)
+    _, n, path = orc.verify_tree_greedy(t.target, t.dtype, t.parents, t.node_tokens, t.max_depth)
+    acc = np.zeros((t.B, t.N), dtype=bool)
+    acc[:, 0] = True
+    for j in range(1, t.N):
+        acc[:, j] = acc[:, t.parents[j]] & t.copied[:, j]
+    depth = gen.tree_depths(t.parents)
+    np.testing.assert_array_equal(n, [depth[acc[i]].max() for i in range(t.B)])
+    for i in range(t.B):
+        assert all(acc[i, p] for p in path[i] if p >= 0)
