@@ -118,7 +118,7 @@ spec_status_t spec_verify_sample(const void *target_logits, spec_dtype_t target_
  * Scratch comes from a fixed 16 MiB (16777216-byte) device array inside the
  * library.  A batch whose spec_workspace_bytes(B, K, V) exceeds that returns
  * SPEC_ERR_UNSUPPORTED (spec_last_error() gives both sizes); B=256, K=5,
- * V=128256 needs 11.9 MB and fits.
+ * V=128256 needs 3.4 MB and fits.
  *
  * The first call on each device (with that device current) looks up the
  * array's device address with cudaGetSymbolAddress, which may load the

@@ -45,27 +45,42 @@
 
 namespace sv {
 
-constexpr int FU_CW = 8;                          // consumer warps
+constexpr int FU_CW = 7;                          // consumer warps
 constexpr int FU_CT = FU_CW * 32;
-constexpr int FU_THREADS = FU_CT + 64;            // + producer warp + finisher warp
-constexpr int FU_FIN_WARP = FU_CW + 1;
+constexpr int FU_THREADS = FU_CT + 96;            // + producer, merger and finisher warps
+constexpr int FU_MERGE_WARP = FU_CW + 1;
+constexpr int FU_FIN_WARP = FU_CW + 2;
 constexpr int FU_STAGE = 16384;
+constexpr int FU_VPT = (FU_STAGE / 16 + FU_CT - 1) / FU_CT;   // 16-byte vectors per consumer thread per stage
 constexpr int FU_NSTAGE = 4;
 constexpr int FU_CTAS_PER_SM = 3;
 constexpr int FU_MAX_GRID = 1024;                 // cursor slots in the workspace
 constexpr int FU_CURSOR_STRIDE = 8;               // one 32-byte sector per cursor
 constexpr int FU_BLK = 256;                       // residual block (elements)
+// Per-sequence flags (units swept, residual units done, ready) share one
+// block of FU_FLAG_STRIDE words, so different sequences' polled words sit in
+// different 32-byte sectors.
+constexpr int FU_FLAG_STRIDE = 8;
+constexpr int FU_IDLE_NS = 256;                   // finisher's sleep between idle polls
+constexpr int FU_WSLOTS = 16;                     // sweep units whose warp partials await their merge
 
 enum : int { KIND_STOP = -1, KIND_SWEEP = 0, KIND_RESID = 1 };
 enum : int { FL_FIRST = 1, FL_LAST = 2, FL_DRAFT = 4, FL_HASQ = 8 };
 
 struct SeqInfo {          // per sequence, written by the accept scan
-  int status, tstar;
   float AP, AQ;           // fl(row max * c) of the stopping target / draft rows
   float iSp, iSq;         // 1 / row sums (relative to AP / AQ); iSq = 1 for probabilities
+  int status, tstar;
   float u1;               // uniform of the replacement / bonus draw
   float pad;
 };
+static_assert(sizeof(SeqInfo) == 32, "SeqInfo: the residual scales are its first 16 bytes");
+
+// The readiness word of a sequence, written (release) by its accept scan:
+// bit 31 set, bit 8 = the sequence is invalid, bits 0-7 = the stopping position.
+__device__ __forceinline__ unsigned fu_ready_word(int status, int tstar) {
+  return 0x80000000u | (status != 0 ? 0x100u : 0u) | static_cast<unsigned>(tstar);
+}
 
 struct FuCtl {            // zeroed before every call (32 bytes reserved)
   unsigned err;           // a wait timed out
@@ -74,8 +89,7 @@ struct FuCtl {            // zeroed before every call (32 bytes reserved)
 static_assert(sizeof(FuCtl) <= 32, "control block must fit its 32-byte slot");
 
 struct StageDesc {
-  int kind, b, unit, e0, n, flags, pad0, pad1;
-  float AP, AQ, iSp, iSq;
+  int kind, b, unit, e0, n, flags, slot, pad;   // slot: partial slot of a sweep unit
 };
 
 struct FusedArgs {
@@ -90,13 +104,12 @@ struct FusedArgs {
   unsigned U;                    // sweep units = B * RB * S
   float c;                       // log2(e) / T
   FuCtl* ctl;
-  unsigned* cnt1;                // [B] sweep units completed
-  unsigned* cnt2;                // [B] residual units completed
-  unsigned* ready;               // [B] 1 once the accept scan has written SeqInfo
+  unsigned* flags;               // [B * FU_FLAG_STRIDE]: per sequence, words 0 (sweep units completed),
+                                 // 1 (residual units completed), 2 (1 once the accept scan wrote SeqInfo)
   unsigned* cursor;              // [FU_MAX_GRID * FU_CURSOR_STRIDE] sweep units claimed per CTA
   SeqInfo* info;                 // [B]
   float* bsum;                   // [B * NB] residual block sums
-  float2* part;                  // [U * FU_CW] sweep warp-partials
+  float4* part;                  // [U] sweep-unit partials (m, hi, lo, 0): sum = hi + lo relative to fl(m*c)
   int32_t* out_tokens;           // [B, K+1]
   int32_t* num_accepted;         // [B]
   int debug_b, debug_t;
@@ -110,8 +123,19 @@ struct FuShared {
   uint64_t empty[FU_NSTAGE];
   StageDesc desc[FU_NSTAGE];
   int unit_cnt[FU_NSTAGE];       // consumer warps done with the work item ending in this stage
+  float4 stage_info[FU_NSTAGE];  // residual stages: the sequence's (AP, AQ, iSp, iSq), copied in with the data
+  float2 wpart[FU_WSLOTS][FU_CW];   // warp partials of completed sweep units, merged by the merger warp
+  int slot_unit[FU_WSLOTS];      // unit id + 1 once its partials are complete; 0 = free
+  int units_issued;              // sweep units the producer issued (-1 while it is running)
+  unsigned res_word;             // readiness word of sequence res_have
+  int res_want;                  // sequence of the producer's next residual unit (-1: none)
+  int res_have;                  // sequence whose readiness word is in res_word (-1: none)
   int abort;
 };
+
+__device__ __forceinline__ unsigned* fu_cnt1(const FusedArgs& a, int b) { return a.flags + b * FU_FLAG_STRIDE; }
+__device__ __forceinline__ unsigned* fu_cnt2(const FusedArgs& a, int b) { return a.flags + b * FU_FLAG_STRIDE + 1; }
+__device__ __forceinline__ unsigned* fu_ready(const FusedArgs& a, int b) { return a.flags + b * FU_FLAG_STRIDE + 2; }
 
 __device__ __forceinline__ bool fu_aborted(const FuShared& sh) {
   return *reinterpret_cast<const volatile int*>(&sh.abort) != 0;
@@ -176,15 +200,15 @@ __device__ __forceinline__ double exp2_d(double x) {
 // max first (packed bf16x2 max), one rescale at most, then exp2 and sums on
 // packed fp32 pairs
 __device__ __forceinline__ void stats_stage_bf16(const uint4* buf, int nvec, int ctid, float c, StatsAcc& acc) {
-  uint4 q[4];
+  uint4 q[FU_VPT];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < FU_VPT; ++k) {
     const int v = ctid + k * FU_CT;
     q[k] = v < nvec ? buf[v] : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
   }
   uint32_t mx = bf16x2_max(bf16x2_max(q[0].x, q[0].y), bf16x2_max(q[0].z, q[0].w));
 #pragma unroll
-  for (int k = 1; k < 4; ++k)
+  for (int k = 1; k < FU_VPT; ++k)
     mx = bf16x2_max(mx, bf16x2_max(bf16x2_max(q[k].x, q[k].y), bf16x2_max(q[k].z, q[k].w)));
   const float vm = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
   if (vm > acc.m) {
@@ -196,7 +220,7 @@ __device__ __forceinline__ void stats_stage_bf16(const uint4* buf, int nvec, int
   const unsigned long long c2 = f2_pack(c, c), n2 = f2_pack(acc.nA, acc.nA);
   unsigned long long s2 = f2_pack(0.f, 0.f);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < FU_VPT; ++k) {
     const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -211,16 +235,16 @@ __device__ __forceinline__ void stats_stage_bf16(const uint4* buf, int nvec, int
 }
 
 __device__ __forceinline__ void stats_stage_f32(const uint4* buf, int nvec, int ctid, float c, StatsAcc& acc) {
-  uint4 q[4];
+  uint4 q[FU_VPT];
   const uint32_t ni = __float_as_uint(kNegInf);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < FU_VPT; ++k) {
     const int v = ctid + k * FU_CT;
     q[k] = v < nvec ? buf[v] : make_uint4(ni, ni, ni, ni);
   }
   float vm = kNegInf;
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
+  for (int k = 0; k < FU_VPT; ++k)
     vm = fmaxf(vm, fmaxf(fmaxf(__uint_as_float(q[k].x), __uint_as_float(q[k].y)),
                          fmaxf(__uint_as_float(q[k].z), __uint_as_float(q[k].w))));
   if (vm > acc.m) {
@@ -232,7 +256,7 @@ __device__ __forceinline__ void stats_stage_f32(const uint4* buf, int nvec, int 
   const unsigned long long c2 = f2_pack(c, c), n2 = f2_pack(acc.nA, acc.nA);
   unsigned long long s2 = f2_pack(0.f, 0.f);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < FU_VPT; ++k) {
     float a0, a1, a2, a3;
     f2_unpack(f2_fma(f2_pack(__uint_as_float(q[k].x), __uint_as_float(q[k].y)), c2, n2), a0, a1);
     f2_unpack(f2_fma(f2_pack(__uint_as_float(q[k].z), __uint_as_float(q[k].w)), c2, n2), a2, a3);
@@ -255,8 +279,8 @@ __device__ __forceinline__ void stats_stage(const uint4* buf, int nvec, int ctid
 // of the stage in its k-th pass (lane l: 8 consecutive elements), so each
 // block sum is one warp reduction of the lanes' sequential 8-element sums.
 template <class TP, class TQ, bool PROBS>
-__device__ __forceinline__ void resid_stage(const unsigned char* buf, const StageDesc& d, int RE, int cw, int lane,
-                                            float c, float* bsum_row) {
+__device__ __forceinline__ void resid_stage(const unsigned char* buf, const StageDesc& d, float4 sc, int RE, int cw,
+                                            int lane, float c, float* bsum_row) {
   using QT = typename std::conditional<PROBS, F32T, TQ>::type;
   const bool has_q = d.flags & FL_HASQ;
   const unsigned char* qb = buf + RE * TP::esz;
@@ -271,7 +295,7 @@ __device__ __forceinline__ void resid_stage(const unsigned char* buf, const Stag
       load8_smem<TP>(buf + g * 8 * TP::esz, zp);
       if (has_q) load8_smem<QT>(qb + g * 8 * QT::esz, zq);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s += resid_w(zp[i], has_q ? zq[i] : 0.f, c, -d.AP, -d.AQ, d.iSp, d.iSq, has_q, PROBS);
+      for (int i = 0; i < 8; ++i) s += resid_w(zp[i], has_q ? zq[i] : 0.f, c, -sc.x, -sc.y, sc.z, sc.w, has_q, PROBS);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -314,81 +338,81 @@ __device__ __forceinline__ ScanInputs scan_inputs(const FusedArgs& a, int b, int
   return in;
 }
 
+// Merge the 8 warp partials (m, s) of a sweep unit into one float-float
+// partial (M, hi, lo): sum = hi + lo relative to fl(M*c).  Lanes 0-7 hold one
+// partial each (the others (-inf, 0)); the whole warp calls it.
+__device__ __forceinline__ float4 merge_unit(float2 p, int lane, float c) {
+  const bool nan = __any_sync(0xffffffffu, p.x != p.x);
+  float M = p.x;
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float hi = 0.f, lo = 0.f;
+  if (!nan && M != kNegInf && p.x != kNegInf) {
+    // fl(m*c) - fl(M*c) is exact in fp32 whenever the factor is not negligible
+    const float f = exp2f(__fmul_rn(p.x, c) - __fmul_rn(M, c));
+    hi = p.y * f;
+    lo = fmaf(p.y, f, -hi);   // the product's rounding error, exactly
+  }
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    const float2 t = two_sum(hi, h2);
+    hi = t.x;
+    lo = lo + (l2 + t.y);
+  }
+  return make_float4(nan ? __int_as_float(0x7fc00000) : M, hi, lo, 0.f);
+}
+
+// Merge the S unit partials of row r of sequence b (one lane): online
+// float-float accumulation relative to the running maximum.  Row r lands in
+// slot r >> 5 of this lane (lane r & 31).
+__device__ __forceinline__ void merge_row(const FusedArgs& a, int b, int r, float (&Ar)[2], double (&Sr)[2],
+                                          int (&st)[2]) {
+  const float4* up = a.part + (static_cast<long long>(b) * a.RB + r) * a.S;
+  float M = kNegInf, hi = 0.f, lo = 0.f;
+  bool bad = false;
+  const float c = a.c;
+#pragma unroll 4
+  for (int j = 0; j < a.S; ++j) {
+    const float4 u = __ldcg(up + j);
+    if (u.x != u.x) {
+      bad = true;
+      continue;
+    }
+    if (u.x == kNegInf) continue;
+    if (u.x > M) {
+      if (M != kNegInf) {
+        const float f = exp2f(__fmul_rn(M, c) - __fmul_rn(u.x, c));
+        const float h = hi * f;
+        lo = fmaf(hi, f, -h) + lo * f;
+        hi = h;
+      }
+      M = u.x;
+    }
+    const float f = exp2f(__fmul_rn(u.x, c) - __fmul_rn(M, c));
+    const float h = u.y * f;
+    const float2 t = two_sum(hi, h);
+    hi = t.x;
+    lo += t.y + fmaf(u.y, f, -h) + u.z * f;
+  }
+  const double acc = static_cast<double>(hi) + static_cast<double>(lo);
+  Ar[r >> 5] = (bad || M == kNegInf) ? 0.f : __fmul_rn(M, c);
+  Sr[r >> 5] = acc;
+  st[r >> 5] = bad ? 2 : (M == kNegInf ? 1 : ((isfinite(acc) && acc > 0.0) ? 0 : 1));
+}
+
 template <class TP, class TQ, bool PROBS>
 __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInputs& in) {
   const int K = a.K, W = K + 1, V = a.V;
-  const int npart = a.S * FU_CW;
   const int x = in.x;
   const float u0 = in.u0;
-  // Merge each row's S x 8 warp partials with the whole warp, eight rows at a
-  // time with their reductions interleaved: lane i holds partial i of each
-  // row; the max is a shuffle tree, the rescaled sums are added in float-float
-  // (two-sum) arithmetic, which is exact to ~1e-14 without slow FP64 chains.
-  // Row r ends up in lane r & 31, slot r >> 5.
   float Ar[2] = {0.f, 0.f};
   double Sr[2] = {0.0, 0.0};
   int st[2] = {1, 1};
-  for (int r0 = 0; r0 < a.RB; r0 += 8) {
-    float M[8], hi[8], lo[8];
-    bool bad[8];
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const int r = r0 + g;
-      const float2* rowp = a.part + (static_cast<long long>(b) * a.RB + r) * npart;
-      M[g] = kNegInf;
-      bad[g] = false;
-      hi[g] = 0.f;
-      lo[g] = 0.f;
-      if (r < a.RB)
-        for (int i = lane; i < npart; i += 32) {
-          const float2 p = __ldcg(rowp + i);
-          if (p.x != p.x) bad[g] = true;
-          else M[g] = fmaxf(M[g], p.x);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int g = 0; g < 8; ++g) M[g] = fmaxf(M[g], __shfl_xor_sync(0xffffffffu, M[g], o));
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const int r = r0 + g;
-      bad[g] = __any_sync(0xffffffffu, bad[g]);
-      if (r < a.RB && !bad[g] && M[g] != kNegInf) {
-        const float AM = __fmul_rn(M[g], a.c);
-        const float2* rowp = a.part + (static_cast<long long>(b) * a.RB + r) * npart;
-        for (int i = lane; i < npart; i += 32) {
-          const float2 p = __ldcg(rowp + i);   // L2 hit (just loaded)
-          if (p.x == kNegInf) continue;
-          // fl(m*c) - fl(M*c) is exact in fp32 whenever the factor is not negligible
-          const float term = p.y * exp2f(__fmul_rn(p.x, a.c) - AM);
-          const float2 t = two_sum(hi[g], term);
-          hi[g] = t.x;
-          lo[g] += t.y;
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const float h2 = __shfl_xor_sync(0xffffffffu, hi[g], o);
-        const float l2 = __shfl_xor_sync(0xffffffffu, lo[g], o);
-        const float2 t = two_sum(hi[g], h2);
-        hi[g] = t.x;
-        lo[g] = lo[g] + (l2 + t.y);
-      }
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const int r = r0 + g;
-      if (r < a.RB && lane == (r & 31)) {
-        const double acc = static_cast<double>(hi[g]) + static_cast<double>(lo[g]);
-        Ar[r >> 5] = (bad[g] || M[g] == kNegInf) ? 0.f : __fmul_rn(M[g], a.c);
-        Sr[r >> 5] = acc;
-        st[r >> 5] = bad[g] ? 2 : (M[g] == kNegInf ? 1 : ((isfinite(acc) && acc > 0.0) ? 0 : 1));
-      }
-    }
-  }
+  // lane r merges row r (and row r + 32 when there are more than 32 rows)
+  if (lane < a.RB) merge_row(a, b, lane, Ar, Sr, st);
+  if (lane + 32 < a.RB) merge_row(a, b, lane + 32, Ar, Sr, st);
 
   // lane t tests position t
   const int t = lane;
@@ -461,7 +485,7 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
   }
   // the warp's writes are ordered before lane 0's release by the warp barrier
   __syncwarp();
-  if (lane == 0) st_release_u32(a.ready + b, 1u);
+  if (lane == 0) st_release_u32(fu_ready(a, b), fu_ready_word(status, tstar));
 }
 
 // ---------------------------------------------------------------------------
@@ -646,10 +670,19 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
   const unsigned RU = static_cast<unsigned>(a.B) * static_cast<unsigned>(a.Sr);
   const unsigned per_seq = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S);
   const int W = a.K + 1;
+  const unsigned G = gridDim.x;
   unsigned next_res = blockIdx.x;
-  // readiness of the next residual unit's sequence: relaxed loads, issued one
-  // unit ahead so their latency overlaps the copies
-  unsigned res_ready = next_res < RU ? ld_relaxed_u32(a.ready + next_res / a.Sr) : 0u;
+  // The finisher warp watches the readiness of the sequence of this CTA's next
+  // residual unit and hands its readiness word (stopping position, validity)
+  // over in shared memory, so the producer never waits on a global load: it
+  // only reads sh.res_have / sh.res_word.
+  auto want_next = [&]() {
+    *reinterpret_cast<volatile int*>(&sh.res_want) = next_res < RU ? static_cast<int>(next_res / a.Sr) : -1;
+  };
+  auto res_is_ready = [&]() -> bool {
+    return next_res < RU && *reinterpret_cast<volatile int*>(&sh.res_have) == static_cast<int>(next_res / a.Sr);
+  };
+  want_next();
 
   auto next_stage = [&]() -> bool {
     if (fu_aborted(sh)) return false;
@@ -663,103 +696,23 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
     if (++stage == FU_NSTAGE) { stage = 0; phase ^= 1u; }
   };
 
-  // own sweep units are blockIdx + k * grid for k = 0, 1, ...; k is claimed on
-  // the CTA's cursor one unit ahead, so the claim's latency is hidden
-  const unsigned G = gridDim.x;
-  auto n_units = [&](unsigned c) { return a.U > c ? (a.U - c + G - 1) / G : 0u; };
-  const unsigned n_own = n_units(blockIdx.x);
-  unsigned own_k = atomicAdd(a.cursor + blockIdx.x * FU_CURSOR_STRIDE, 1u);
-  unsigned victim = 0, steal_fails = 0;
-  bool stealing = true;
-  bool ok = true;
-  while (ok) {
-    long long rid = -1, uid = -1;
-    if (next_res < RU && res_ready) {
-      rid = next_res;
-      next_res += G;
-    } else if (own_k < n_own) {
-      uid = blockIdx.x + static_cast<long long>(own_k) * G;
-      own_k = atomicAdd(a.cursor + blockIdx.x * FU_CURSOR_STRIDE, 1u);
-    } else if (stealing) {
-      // take the next unclaimed unit of another CTA (victims in a fixed order)
-      victim = (victim + 1) % G;
-      const unsigned v = (blockIdx.x + victim * 97u) % G;
-      if (v != blockIdx.x) {
-        const unsigned k = atomicAdd(a.cursor + v * FU_CURSOR_STRIDE, 1u);
-        if (k < n_units(v)) {
-          uid = v + static_cast<long long>(k) * G;
-          steal_fails = 0;
-        } else if (++steal_fails >= 16) {
-          stealing = false;
-        }
-      }
-      if (victim + 1 >= G) stealing = false;
-      if (uid < 0) {
-        res_ready = next_res < RU ? ld_relaxed_u32(a.ready + next_res / a.Sr) : 0u;
-        continue;
-      }
-    } else if (next_res < RU) {
-      // sweep done: wait for the next residual unit's sequence
-      const uint64_t t0 = global_ns();
-      bool rdy = false;
-      while (!(rdy = ld_relaxed_u32(a.ready + next_res / a.Sr) != 0u)) {
-        if (fu_aborted(sh) || global_ns() - t0 > a.timeout_ns) break;
-        __nanosleep(200);
-      }
-      if (!rdy) {
-        fu_fail(sh, a.ctl, 2u);
-        break;
-      }
-      rid = next_res;
-      next_res += G;
-    } else {
-      break;
-    }
-    res_ready = next_res < RU ? ld_relaxed_u32(a.ready + next_res / a.Sr) : 0u;
-    if (uid >= 0) {
-      const unsigned u = static_cast<unsigned>(uid);
-      const int b = static_cast<int>(u / per_seq);
-      const unsigned rem = u - static_cast<unsigned>(b) * per_seq;
-      const int row = static_cast<int>(rem / a.S);
-      const int j = static_cast<int>(rem - static_cast<unsigned>(row) * a.S);
-      const bool is_draft = row >= W;
-      const int esz = is_draft ? QT::esz : TP::esz;
-      const unsigned char* src =
-          is_draft ? a.draft + ((static_cast<long long>(b) * a.K + (row - W)) * a.V) * esz
-                   : a.target + ((static_cast<long long>(b) * W + row) * a.V) * esz;
-      const int e0 = j * a.L, e1 = min(a.V, e0 + a.L);
-      const uint32_t bytes = static_cast<uint32_t>((e1 - e0) * esz);
-      for (uint32_t off = 0; off < bytes; off += FU_STAGE) {
-        const uint32_t n = min(static_cast<uint32_t>(FU_STAGE), bytes - off);
-        if (!next_stage()) { ok = false; break; }
-        StageDesc& d = sh.desc[stage];
-        d.kind = KIND_SWEEP;
-        d.b = b;
-        d.unit = static_cast<int>(u);
-        d.e0 = e0 + static_cast<int>(off) / esz;
-        d.n = static_cast<int>(n);   // bytes for sweep stages
-        d.flags = (off == 0 ? FL_FIRST : 0) | (off + n >= bytes ? FL_LAST : 0) | (is_draft ? FL_DRAFT : 0);
-        mbar_arrive_expect_tx(&sh.full[stage], n);
-        bulk_g2s(ring + stage * FU_STAGE, src + static_cast<long long>(e0) * esz + off, n, &sh.full[stage]);
-        last_parity[stage] = static_cast<int>(phase);
-        advance();
-      }
-      continue;
-    }
-    // residual unit rid = b * Sr + j of a ready sequence
-    __threadfence();   // acquire side of the readiness flag: SeqInfo is visible
+  // The next residual unit rid = b * Sr + j (its sequence is ready).  Its
+  // stages may go between two stages of a sweep unit: the consumers keep their
+  // sweep accumulators across them.  The sequence's residual scales (the first
+  // 16 bytes of its SeqInfo) are copied into each stage's info slot by the
+  // bulk-copy engine together with the row data.
+  auto issue_resid = [&]() -> bool {
+    const long long rid = next_res;
+    next_res += G;
     const int b = static_cast<int>(rid / a.Sr);
     const int j = static_cast<int>(rid - static_cast<long long>(b) * a.Sr);
-    SeqInfo inf;
-    {
-      const int* src = reinterpret_cast<const int*>(a.info + b);
-      int* dst = reinterpret_cast<int*>(&inf);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dst[i] = __ldcg(src + i);
-    }
-    if (inf.status != 0) {
+    __threadfence_block();   // the finisher stored res_word before res_have
+    const unsigned word = *reinterpret_cast<volatile unsigned*>(&sh.res_word);
+    want_next();
+    const int tstar = static_cast<int>(word & 0xffu);
+    if (word & 0x100u) {
       // invalid sequence: a data-less stage, so the arrival is still counted
-      if (!next_stage()) break;
+      if (!next_stage()) return false;
       StageDesc& d = sh.desc[stage];
       d.kind = KIND_RESID;
       d.b = b;
@@ -770,16 +723,20 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
       mbar_arrive(&sh.full[stage]);
       last_parity[stage] = -1;   // the stage was released: its previous copy has landed
       advance();
-      continue;
+      return true;
     }
-    const bool has_q = inf.tstar < a.K;
-    const unsigned char* prow = a.target + ((static_cast<long long>(b) * W + inf.tstar) * a.V) * TP::esz;
+    // The scan's SeqInfo stores are ordered before its release of the
+    // readiness word, which the finisher acquired before handing it over; the
+    // proxy fence orders the bulk-copy engine's reads after that.
+    fence_proxy_async_global();
+    const bool has_q = tstar < a.K;
+    const unsigned char* prow = a.target + ((static_cast<long long>(b) * W + tstar) * a.V) * TP::esz;
     const unsigned char* qrow =
-        has_q ? a.draft + ((static_cast<long long>(b) * a.K + inf.tstar) * a.V) * QT::esz : nullptr;
+        has_q ? a.draft + ((static_cast<long long>(b) * a.K + tstar) * a.V) * QT::esz : nullptr;
     const int e0 = j * a.Lr, e1 = min(a.V, e0 + a.Lr);
     for (int e = e0; e < e1; e += a.RE) {
       const int n = min(a.RE, e1 - e);
-      if (!next_stage()) { ok = false; break; }
+      if (!next_stage()) return false;
       StageDesc& d = sh.desc[stage];
       d.kind = KIND_RESID;
       d.b = b;
@@ -787,19 +744,136 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
       d.e0 = e;
       d.n = n;   // elements for residual stages
       d.flags = (e == e0 ? FL_FIRST : 0) | (e + n >= e1 ? FL_LAST : 0) | (has_q ? FL_HASQ : 0);
-      d.AP = inf.AP;
-      d.AQ = inf.AQ;
-      d.iSp = inf.iSp;
-      d.iSq = inf.iSq;
       const uint32_t bp = static_cast<uint32_t>(n * TP::esz), bq = has_q ? static_cast<uint32_t>(n * QT::esz) : 0u;
-      mbar_arrive_expect_tx(&sh.full[stage], bp + bq);
+      mbar_arrive_expect_tx(&sh.full[stage], bp + bq + 16u);
       unsigned char* dst = ring + stage * FU_STAGE;
       bulk_g2s(dst, prow + static_cast<long long>(e) * TP::esz, bp, &sh.full[stage]);
       if (has_q) bulk_g2s(dst + a.RE * TP::esz, qrow + static_cast<long long>(e) * QT::esz, bq, &sh.full[stage]);
+      bulk_g2s(&sh.stage_info[stage], a.info + b, 16u, &sh.full[stage]);
       last_parity[stage] = static_cast<int>(phase);
       advance();
     }
+    return true;
+  };
+
+  // Sweep units take partial slots in turn; a slot is free again once the
+  // finisher warp has read (and then merges) the partials left in it.
+  int unit_seq = 0;
+
+  // Own sweep units are blockIdx + k * grid for k = 0, 1, ...; k is claimed on
+  // the CTA's cursor one unit ahead, so the claim's latency is hidden.  The
+  // loop acquires one ring stage at a time and then decides what fills it: the
+  // next residual unit if its sequence is ready, else the next stage of the
+  // current sweep unit.
+  auto n_units = [&](unsigned c) { return a.U > c ? (a.U - c + G - 1) / G : 0u; };
+  const unsigned n_own = n_units(blockIdx.x);
+  unsigned own_k = atomicAdd(a.cursor + blockIdx.x * FU_CURSOR_STRIDE, 1u);
+  unsigned victim = 0, steal_fails = 0;
+  bool stealing = true;
+  bool ok = true;
+  // current sweep unit and its partial slot
+  bool have = false;
+  unsigned u = 0;
+  int slot = 0;
+  int b = 0, e0 = 0, esz = 0;
+  bool is_draft = false;
+  const unsigned char* src = nullptr;
+  uint32_t bytes = 0, off = 0;
+  while (ok) {
+    if (!next_stage()) break;
+    if (res_is_ready()) {
+      ok = issue_resid();
+      continue;
+    }
+    if (!have) {
+      long long uid = -1;
+      while (uid < 0) {
+        if (own_k < n_own) {
+          uid = blockIdx.x + static_cast<long long>(own_k) * G;
+          own_k = atomicAdd(a.cursor + blockIdx.x * FU_CURSOR_STRIDE, 1u);
+        } else if (stealing) {
+          // take the next unclaimed unit of another CTA (victims in a fixed order)
+          victim = (victim + 1) % G;
+          const unsigned v = (blockIdx.x + victim * 97u) % G;
+          if (v != blockIdx.x) {
+            const unsigned k = atomicAdd(a.cursor + v * FU_CURSOR_STRIDE, 1u);
+            if (k < n_units(v)) {
+              uid = v + static_cast<long long>(k) * G;
+              steal_fails = 0;
+            } else if (++steal_fails >= 16) {
+              stealing = false;
+            }
+          }
+          if (victim + 1 >= G) stealing = false;
+        } else {
+          break;
+        }
+      }
+      if (uid < 0) {
+        // no sweep work left: the remaining residual units, as their sequences become ready
+        if (next_res >= RU) break;
+        const uint64_t t0 = global_ns();
+        bool rdy = false;
+        while (!(rdy = res_is_ready())) {
+          if (fu_aborted(sh) || global_ns() - t0 > a.timeout_ns) break;
+          __nanosleep(100);
+        }
+        if (!rdy) {
+          fu_fail(sh, a.ctl, 2u);
+          break;
+        }
+        ok = issue_resid();
+        continue;
+      }
+      u = static_cast<unsigned>(uid);
+      b = static_cast<int>(u / per_seq);
+      const unsigned rem = u - static_cast<unsigned>(b) * per_seq;
+      const int row = static_cast<int>(rem / a.S);
+      const int j = static_cast<int>(rem - static_cast<unsigned>(row) * a.S);
+      is_draft = row >= W;
+      esz = is_draft ? QT::esz : TP::esz;
+      src = is_draft ? a.draft + ((static_cast<long long>(b) * a.K + (row - W)) * a.V) * esz
+                     : a.target + ((static_cast<long long>(b) * W + row) * a.V) * esz;
+      e0 = j * a.L;
+      bytes = static_cast<uint32_t>((min(a.V, e0 + a.L) - e0) * esz);
+      off = 0;
+      have = true;
+      slot = unit_seq % FU_WSLOTS;
+      ++unit_seq;
+      // the slot's previous unit (FU_WSLOTS units back) must have been read
+      if (*reinterpret_cast<volatile int*>(&sh.slot_unit[slot]) != 0) {
+        const uint64_t t0 = global_ns();
+        while (*reinterpret_cast<volatile int*>(&sh.slot_unit[slot]) != 0) {
+          if (fu_aborted(sh) || global_ns() - t0 > a.timeout_ns) {
+            fu_fail(sh, a.ctl, 16u);
+            ok = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (!ok) break;
+      }
+    }
+    const uint32_t n = min(static_cast<uint32_t>(FU_STAGE), bytes - off);
+    StageDesc& d = sh.desc[stage];
+    d.kind = KIND_SWEEP;
+    d.b = b;
+    d.unit = static_cast<int>(u);
+    d.e0 = e0 + static_cast<int>(off) / esz;
+    d.n = static_cast<int>(n);   // bytes for sweep stages
+    d.flags = (off == 0 ? FL_FIRST : 0) | (off + n >= bytes ? FL_LAST : 0) | (is_draft ? FL_DRAFT : 0);
+    d.slot = slot;
+    mbar_arrive_expect_tx(&sh.full[stage], n);
+    bulk_g2s(ring + stage * FU_STAGE, src + static_cast<long long>(e0) * esz + off, n, &sh.full[stage]);
+    last_parity[stage] = static_cast<int>(phase);
+    advance();
+    off += n;
+    if (off >= bytes) have = false;
   }
+  // the finisher may leave once it has merged this many units (a unit claimed
+  // but never issued is not counted)
+  *reinterpret_cast<volatile int*>(&sh.units_issued) = have && off == 0 ? unit_seq - 1 : unit_seq;
+  *reinterpret_cast<volatile int*>(&sh.res_want) = -1;
   // stop marker for the consumers
   if (next_stage()) {
     sh.desc[stage].kind = KIND_STOP;
@@ -834,7 +908,7 @@ __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& s
     }
     const StageDesc d = sh.desc[stage];
     if (d.kind == KIND_STOP) break;
-    if (d.flags & FL_FIRST) sacc.init();
+    if (d.kind == KIND_SWEEP && (d.flags & FL_FIRST)) sacc.init();
     const int cur = stage;
     const unsigned char* buf = ring + stage * FU_STAGE;
     if (d.kind == KIND_SWEEP) {
@@ -844,7 +918,8 @@ __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& s
         stats_stage<TP>(reinterpret_cast<const uint4*>(buf), d.n >> 4, ctid, a.c, sacc);
       }
     } else if (d.n > 0) {
-      resid_stage<TP, TQ, PROBS>(buf, d, a.RE, cw, lane, a.c, a.bsum + static_cast<long long>(d.b) * a.NB);
+      resid_stage<TP, TQ, PROBS>(buf, d, sh.stage_info[cur], a.RE, cw, lane, a.c,
+                                 a.bsum + static_cast<long long>(d.b) * a.NB);
     }
     if (++stage == FU_NSTAGE) { stage = 0; phase ^= 1u; }
     if (!(d.flags & FL_LAST)) {
@@ -852,27 +927,100 @@ __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& s
       if (lane == 0) mbar_arrive(&sh.empty[cur]);
       continue;
     }
-    // End of a work item: every warp writes its partial; the warps count
-    // themselves in shared memory and the last one adds the item to the
-    // sequence's counter (fire-and-forget, release ordered).
+    // End of a work item: every warp leaves its partial in shared memory (a
+    // sweep unit's slot) and counts itself there.  The last one releases the
+    // stage and hands the unit on: a sweep unit to the finisher warp, which
+    // merges the partials and adds the unit to the sequence's counter off the
+    // consumers' path; a residual unit straight to its counter
+    // (fire-and-forget, release ordered).
     if (d.kind == KIND_SWEEP) sacc.warp_reduce(a.c);
     else __syncwarp();
+    int prev = 0;
     if (lane == 0) {
-      if (d.kind == KIND_SWEEP) a.part[static_cast<long long>(d.unit) * FU_CW + cw] = sacc.pack();
+      if (d.kind == KIND_SWEEP) sh.wpart[d.slot][cw] = sacc.pack();
       __threadfence_block();
-      const int prev = atomicAdd(&sh.unit_cnt[cur], 1);
-      if (prev == FU_CW - 1) {
-        sh.unit_cnt[cur] = 0;   // the slot's next item starts only after this warp releases it
-        // The other warps' partial stores are ordered before their shared-memory
-        // increments (block fence); this warp observed those increments, and its
-        // block fence plus the gpu-scope release of the reduction carry all of
-        // them to whoever acquires the counter.
-        __threadfence_block();
-        red_release_add_u32(d.kind == KIND_SWEEP ? a.cnt1 + d.b : a.cnt2 + d.b, 1u);
+      prev = atomicAdd(&sh.unit_cnt[cur], 1);
+    }
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    if (prev == FU_CW - 1 && lane == 0) {
+      sh.unit_cnt[cur] = 0;   // the slot's next item starts only after this warp releases it
+      // the other warps' partials are ordered before their increments, which
+      // this warp observed; its block fence orders the hand-over after them
+      __threadfence_block();
+      if (d.kind == KIND_SWEEP) {
+        *reinterpret_cast<volatile int*>(&sh.slot_unit[d.slot]) = d.unit + 1;
+      } else {
+        red_release_add_u32(fu_cnt2(a, d.b), 1u);
       }
+      mbar_arrive(&sh.empty[cur]);
+    } else if (lane == 0) {
       mbar_arrive(&sh.empty[cur]);
     }
     __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// merger (one warp): merges the warp partials of this CTA's completed sweep
+// units and hands the readiness word of the producer's next residual sequence
+// over, off the consumers' and the producer's paths
+// ---------------------------------------------------------------------------
+__device__ void fu_merger(const FusedArgs& a, FuShared& sh, int lane) {
+  const unsigned per_seq_units = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S);
+  int merged = 0;
+  uint64_t last_progress = global_ns();
+  for (;;) {
+    const int want = *reinterpret_cast<volatile int*>(&sh.res_want);
+    const int issued = *reinterpret_cast<volatile int*>(&sh.units_issued);
+    if (want < 0 && issued >= 0 && merged >= issued) break;
+    bool progress = false;
+    // the readiness poll is issued first and read after the merges
+    const bool need_res = want >= 0 && *reinterpret_cast<volatile int*>(&sh.res_have) != want;
+    unsigned v = 0;
+    if (lane == 0 && need_res) v = ld_relaxed_u32(fu_ready(a, want));
+    {
+      const int su = lane < FU_WSLOTS ? *reinterpret_cast<volatile int*>(&sh.slot_unit[lane]) : 0;
+      unsigned m = __ballot_sync(0xffffffffu, su != 0);
+      while (m) {
+        const int sl = __ffs(m) - 1;
+        m &= m - 1u;
+        const int unit = __shfl_sync(0xffffffffu, su, sl) - 1;
+        __threadfence_block();
+        const float2 wp = lane < FU_CW ? sh.wpart[sl][lane] : make_float2(kNegInf, 0.f);
+        __syncwarp();
+        __threadfence_block();
+        if (lane == 0) *reinterpret_cast<volatile int*>(&sh.slot_unit[sl]) = 0;   // partials are in registers
+        const float4 u = merge_unit(wp, lane, a.c);
+        if (lane == 0) {
+          a.part[unit] = u;
+          __threadfence_block();
+          red_release_add_u32(fu_cnt1(a, static_cast<int>(static_cast<unsigned>(unit) / per_seq_units)), 1u);
+        }
+        ++merged;
+        progress = true;
+      }
+    }
+    const unsigned v_res = __shfl_sync(0xffffffffu, v, 0);
+    if (need_res && v_res != 0u) {
+      __threadfence();   // acquire: the scan's SeqInfo stores are visible from here on
+      if (lane == 0) {
+        *reinterpret_cast<volatile unsigned*>(&sh.res_word) = v_res;
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(&sh.res_have) = want;
+      }
+      progress = true;
+    }
+    __syncwarp();
+    if (progress) {
+      last_progress = global_ns();
+      continue;
+    }
+    const bool stop = __any_sync(0xffffffffu, fu_aborted(sh) || global_ns() - last_progress > 4 * a.timeout_ns);
+    if (stop) {
+      if (lane == 0) fu_fail(sh, a.ctl, 64u);
+      break;
+    }
+    __nanosleep(64);
   }
 }
 
@@ -892,26 +1040,25 @@ __device__ void fu_finisher(const FusedArgs& a, FuShared& sh, int lane) {
   uint64_t last_progress = global_ns();
   while (bs < static_cast<unsigned>(a.B) || bp < static_cast<unsigned>(a.B)) {
     bool progress = false;
-    if (bs < static_cast<unsigned>(a.B)) {
-      unsigned v = 0;
-      if (lane == 0) v = ld_relaxed_u32(a.cnt1 + bs);
-      if (__shfl_sync(0xffffffffu, v, 0) == per_seq) {
-        __threadfence();
-        finish_scan<TP, TQ, PROBS>(a, static_cast<int>(bs), lane, in);
-        bs += G;
-        if (bs < static_cast<unsigned>(a.B)) in = scan_inputs<TP, TQ, PROBS>(a, static_cast<int>(bs), lane);
-        progress = true;
-      }
+    // both polls in one round (lane 1: the next scan's sweep counter, lane 2:
+    // the next pick's residual counter)
+    unsigned v = 0;
+    if (lane == 1 && bs < static_cast<unsigned>(a.B)) v = ld_relaxed_u32(fu_cnt1(a, static_cast<int>(bs)));
+    if (lane == 2 && bp < static_cast<unsigned>(a.B)) v = ld_relaxed_u32(fu_cnt2(a, static_cast<int>(bp)));
+    const unsigned v_scan = __shfl_sync(0xffffffffu, v, 1);
+    const unsigned v_pick = __shfl_sync(0xffffffffu, v, 2);
+    if (bs < static_cast<unsigned>(a.B) && v_scan == per_seq) {
+      __threadfence();
+      finish_scan<TP, TQ, PROBS>(a, static_cast<int>(bs), lane, in);
+      bs += G;
+      if (bs < static_cast<unsigned>(a.B)) in = scan_inputs<TP, TQ, PROBS>(a, static_cast<int>(bs), lane);
+      progress = true;
     }
-    if (bp < static_cast<unsigned>(a.B)) {
-      unsigned v = 0;
-      if (lane == 0) v = ld_relaxed_u32(a.cnt2 + bp);
-      if (__shfl_sync(0xffffffffu, v, 0) == static_cast<unsigned>(a.Sr)) {
-        __threadfence();
-        finish_pick<TP, TQ, PROBS>(a, static_cast<int>(bp), lane);
-        bp += G;
-        progress = true;
-      }
+    if (bp < static_cast<unsigned>(a.B) && v_pick == static_cast<unsigned>(a.Sr)) {
+      __threadfence();
+      finish_pick<TP, TQ, PROBS>(a, static_cast<int>(bp), lane);
+      bp += G;
+      progress = true;
     }
     __syncwarp();
     if (progress) {
@@ -923,7 +1070,7 @@ __device__ void fu_finisher(const FusedArgs& a, FuShared& sh, int lane) {
       if (lane == 0) fu_fail(sh, a.ctl, 32u);
       break;
     }
-    __nanosleep(256);
+    __nanosleep(FU_IDLE_NS);
   }
 }
 
@@ -945,12 +1092,21 @@ __global__ void __launch_bounds__(FU_THREADS, FU_CTAS_PER_SM) fused_sample_kerne
       sh.unit_cnt[s] = 0;
     }
     sh.abort = 0;
+    sh.res_have = -1;
+    sh.units_issued = -1;
+    for (int i = 0; i < FU_WSLOTS; ++i) sh.slot_unit[i] = 0;
+    // the sequence of this CTA's first residual unit, set before any warp
+    // starts, so the finisher cannot leave before the producer asks for it
+    const unsigned RU = static_cast<unsigned>(a.B) * static_cast<unsigned>(a.Sr);
+    sh.res_want = blockIdx.x < RU ? static_cast<int>(blockIdx.x / a.Sr) : -1;
     mbar_fence_init();
   }
   __syncthreads();
 
   if (warp == 0) {
     if (lane == 0) fu_producer<TP, TQ, PROBS>(a, ring, sh);
+  } else if (warp == FU_MERGE_WARP) {
+    fu_merger(a, sh, lane);
   } else if (warp == FU_FIN_WARP) {
     fu_finisher<TP, TQ, PROBS>(a, sh, lane);
   } else {

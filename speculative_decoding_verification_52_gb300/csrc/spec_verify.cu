@@ -295,21 +295,21 @@ int finish_max_cluster(int dev) {
 }
 
 // Workspace of the fused sampling kernel:
-//   [FuCtl | cnt1[B] | cnt2[B] | ready[B] | cursor[1024 x 8]]   zeroed per call
-//   [info[B] | bsum[B * ceil(V/256)] | part[rows * S * 8]]
+//   [FuCtl | flags[B * FU_FLAG_STRIDE] | cursor[1024 x 8]]   zeroed per call
+//   [info[B] | bsum[B * ceil(V/256)] | part[rows * S] (float4)]
 struct FusedLayout {
   size_t cursor_off, zero_bytes, info_off, bsum_off, part_off, total;
 };
 FusedLayout fused_layout(int B, int K, int V) {
   FusedLayout l{};
   const size_t nb = static_cast<size_t>((V + FU_BLK - 1) / FU_BLK);
-  l.cursor_off = align_up(32 + 12u * static_cast<size_t>(B), 32);
+  l.cursor_off = align_up(32 + sizeof(unsigned) * FU_FLAG_STRIDE * static_cast<size_t>(B), 32);
   l.zero_bytes = l.cursor_off + sizeof(unsigned) * FU_MAX_GRID * FU_CURSOR_STRIDE;
   l.info_off = l.zero_bytes;
   l.bsum_off = align_up(l.info_off + sizeof(SeqInfo) * static_cast<size_t>(B), 16);
   l.part_off = align_up(l.bsum_off + sizeof(float) * static_cast<size_t>(B) * nb, 16);
   const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(2 * K + 1);
-  l.total = align_up(l.part_off + rows * static_cast<size_t>(max_slices(V)) * FU_CW * sizeof(float2), 256);
+  l.total = align_up(l.part_off + rows * static_cast<size_t>(max_slices(V)) * sizeof(float4), 256);
   return l;
 }
 
@@ -382,13 +382,11 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   a.c = c;
   a.NB = ceil_div(V, FU_BLK);
   a.ctl = reinterpret_cast<FuCtl*>(w);
-  a.cnt1 = reinterpret_cast<unsigned*>(w + 32);
-  a.cnt2 = a.cnt1 + B;
-  a.ready = a.cnt2 + B;
+  a.flags = reinterpret_cast<unsigned*>(w + 32);
   a.cursor = reinterpret_cast<unsigned*>(w + lay.cursor_off);
   a.info = reinterpret_cast<SeqInfo*>(w + lay.info_off);
   a.bsum = reinterpret_cast<float*>(w + lay.bsum_off);
-  a.part = reinterpret_cast<float2*>(w + lay.part_off);
+  a.part = reinterpret_cast<float4*>(w + lay.part_off);
   a.out_tokens = out;
   a.num_accepted = nacc;
   a.debug_b = debug_b;
@@ -629,7 +627,7 @@ spec_status_t sample_entry(const void* target, spec_dtype_t tdt, const void* dra
 // ---------------------------------------------------------------------------
 // A file-scope device array stands in for the caller's workspace, so that call
 // allocates nothing.  It holds kNoallocScratchBytes (16 MiB: the B=256, K=5,
-// V=128256 batch needs 11.9 MB).  Every call on a device uses the same array:
+// V=128256 batch needs 3.4 MB).  Every call on a device uses the same array:
 // calls that may overlap on the GPU (other streams, other host threads) race
 // on it.  The part of it that must start at zero (the fused kernel's control
 // block and counters) is cleared on the call's stream by every call, exactly as

@@ -22,7 +22,7 @@ def test_noalloc_rejects_oversized_batch_on_host():
     build_mod.build()
     L = B.lib()
     P = ctypes.c_void_p
-    Bn, K, V = 512, 8, 151936
+    Bn, K, V = 2048, 8, 151936
     assert L.spec_workspace_bytes(Bn, K, V) > NOALLOC_BYTES
     st = L.spec_verify_sample_noalloc(P(1 << 20), B.SPEC_BF16, P(1 << 21), B.SPEC_BF16, B.SPEC_DRAFT_LOGITS,
                                       P(1 << 22), P(1 << 23), 0.7, Bn, K, V, P(1 << 24), P(1 << 25), None)
