@@ -3,9 +3,8 @@
 // exactness rule"; "Speculative decoding: draft, verify, repeat", steps 1-3;
 // "Speculative Decoding: from idea to SOTA", section 3).
 //
-// Work items (both kinds dealt round-robin to the CTAs; a CTA claims its own
-// sweep units through a private cursor, and a CTA that has run out of its own
-// steals the last units of others, so slow CTAs do not delay the end):
+// Work items (sweep units claimed from one counter in unit order; residual
+// units dealt round-robin to the CTAs):
 //   sweep unit    (sequence b, row r, slice j): softmax-normaliser partials
 //                 (max m, sum 2^(z*c - fl(m*c))) of one slice of one target or
 //                 draft row, numbered sequence-major so the batch is swept in
@@ -54,8 +53,7 @@ constexpr int FU_STAGE = 16384;
 constexpr int FU_VPT = (FU_STAGE / 16 + FU_CT - 1) / FU_CT;   // 16-byte vectors per consumer thread per stage
 constexpr int FU_NSTAGE = 4;
 constexpr int FU_CTAS_PER_SM = 3;
-constexpr int FU_MAX_GRID = 1024;                 // cursor slots in the workspace
-constexpr int FU_CURSOR_STRIDE = 8;               // one 32-byte sector per cursor
+constexpr int FU_MAX_GRID = 1024;                 // persistent grid cap
 constexpr int FU_BLK = 256;                       // residual block (elements)
 // Per-sequence flags (units swept, residual units done, ready) share one
 // block of FU_FLAG_STRIDE words, so different sequences' polled words sit in
@@ -85,6 +83,7 @@ __device__ __forceinline__ unsigned fu_ready_word(int status, int tstar) {
 struct FuCtl {            // zeroed before every call (32 bytes reserved)
   unsigned err;           // a wait timed out
   unsigned done;          // CTAs that have left
+  unsigned claim;         // sweep units claimed by the producers, in unit order
 };
 static_assert(sizeof(FuCtl) <= 32, "control block must fit its 32-byte slot");
 
@@ -106,7 +105,6 @@ struct FusedArgs {
   FuCtl* ctl;
   unsigned* flags;               // [B * FU_FLAG_STRIDE]: per sequence, words 0 (sweep units completed),
                                  // 1 (residual units completed), 2 (1 once the accept scan wrote SeqInfo)
-  unsigned* cursor;              // [FU_MAX_GRID * FU_CURSOR_STRIDE] sweep units claimed per CTA
   SeqInfo* info;                 // [B]
   float* bsum;                   // [B * NB] residual block sums
   float4* part;                  // [U] sweep-unit partials (m, hi, lo, 0): sum = hi + lo relative to fl(m*c)
@@ -760,16 +758,12 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
   // finisher warp has read (and then merges) the partials left in it.
   int unit_seq = 0;
 
-  // Own sweep units are blockIdx + k * grid for k = 0, 1, ...; k is claimed on
-  // the CTA's cursor one unit ahead, so the claim's latency is hidden.  The
-  // loop acquires one ring stage at a time and then decides what fills it: the
-  // next residual unit if its sequence is ready, else the next stage of the
-  // current sweep unit.
-  auto n_units = [&](unsigned c) { return a.U > c ? (a.U - c + G - 1) / G : 0u; };
-  const unsigned n_own = n_units(blockIdx.x);
-  unsigned own_k = atomicAdd(a.cursor + blockIdx.x * FU_CURSOR_STRIDE, 1u);
-  unsigned victim = 0, steal_fails = 0;
-  bool stealing = true;
+  // Sweep units are claimed from one counter, in unit order (sequence-major),
+  // one unit ahead so the claim's latency is hidden.  The loop acquires one
+  // ring stage at a time and then decides what fills it: the next residual
+  // unit if its sequence is ready, else the next stage of the current sweep
+  // unit.
+  unsigned next_claim = atomicAdd(&a.ctl->claim, 1u);
   bool ok = true;
   // current sweep unit and its partial slot
   bool have = false;
@@ -787,27 +781,9 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
     }
     if (!have) {
       long long uid = -1;
-      while (uid < 0) {
-        if (own_k < n_own) {
-          uid = blockIdx.x + static_cast<long long>(own_k) * G;
-          own_k = atomicAdd(a.cursor + blockIdx.x * FU_CURSOR_STRIDE, 1u);
-        } else if (stealing) {
-          // take the next unclaimed unit of another CTA (victims in a fixed order)
-          victim = (victim + 1) % G;
-          const unsigned v = (blockIdx.x + victim * 97u) % G;
-          if (v != blockIdx.x) {
-            const unsigned k = atomicAdd(a.cursor + v * FU_CURSOR_STRIDE, 1u);
-            if (k < n_units(v)) {
-              uid = v + static_cast<long long>(k) * G;
-              steal_fails = 0;
-            } else if (++steal_fails >= 16) {
-              stealing = false;
-            }
-          }
-          if (victim + 1 >= G) stealing = false;
-        } else {
-          break;
-        }
+      if (next_claim < a.U) {
+        uid = next_claim;
+        next_claim = atomicAdd(&a.ctl->claim, 1u);
       }
       if (uid < 0) {
         // no sweep work left: the remaining residual units, as their sequences become ready

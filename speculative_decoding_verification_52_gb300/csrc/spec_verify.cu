@@ -295,16 +295,15 @@ int finish_max_cluster(int dev) {
 }
 
 // Workspace of the fused sampling kernel:
-//   [FuCtl | flags[B * FU_FLAG_STRIDE] | cursor[1024 x 8]]   zeroed per call
+//   [FuCtl | flags[B * FU_FLAG_STRIDE]]   zeroed per call
 //   [info[B] | bsum[B * ceil(V/256)] | part[rows * S] (float4)]
 struct FusedLayout {
-  size_t cursor_off, zero_bytes, info_off, bsum_off, part_off, total;
+  size_t zero_bytes, info_off, bsum_off, part_off, total;
 };
 FusedLayout fused_layout(int B, int K, int V) {
   FusedLayout l{};
   const size_t nb = static_cast<size_t>((V + FU_BLK - 1) / FU_BLK);
-  l.cursor_off = align_up(32 + sizeof(unsigned) * FU_FLAG_STRIDE * static_cast<size_t>(B), 32);
-  l.zero_bytes = l.cursor_off + sizeof(unsigned) * FU_MAX_GRID * FU_CURSOR_STRIDE;
+  l.zero_bytes = align_up(32 + sizeof(unsigned) * FU_FLAG_STRIDE * static_cast<size_t>(B), 32);
   l.info_off = l.zero_bytes;
   l.bsum_off = align_up(l.info_off + sizeof(SeqInfo) * static_cast<size_t>(B), 16);
   l.part_off = align_up(l.bsum_off + sizeof(float) * static_cast<size_t>(B) * nb, 16);
@@ -383,7 +382,6 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   a.NB = ceil_div(V, FU_BLK);
   a.ctl = reinterpret_cast<FuCtl*>(w);
   a.flags = reinterpret_cast<unsigned*>(w + 32);
-  a.cursor = reinterpret_cast<unsigned*>(w + lay.cursor_off);
   a.info = reinterpret_cast<SeqInfo*>(w + lay.info_off);
   a.bsum = reinterpret_cast<float*>(w + lay.bsum_off);
   a.part = reinterpret_cast<float4*>(w + lay.part_off);

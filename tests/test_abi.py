@@ -25,19 +25,18 @@ def test_exports_every_declared_symbol(L):
 
 def test_workspace_sizes(L):
     # control block (32 B) + per-sequence counters and readiness flags (one
-    # 32-byte block each) + 1024
-    # per-CTA claim cursors (32 B each), per-sequence info (32 B), residual
+    # 32-byte block each), per-sequence info (32 B), residual
     # block sums (ceil(V/256) floats per sequence), and one 16-byte partial per
     # sweep unit (rows x at most ceil(V/2048) slices)
     def al(x, a):
         return (x + a - 1) // a * a
     B_, K_, V_ = 256, 5, 128256
-    zero = al(32 + 32 * B_, 32) + 1024 * 32   # 8 flag words per sequence
+    zero = al(32 + 32 * B_, 32)   # 8 flag words per sequence
     bsum = al(zero + 32 * B_, 16)
     part = al(bsum + 4 * B_ * (-(-V_ // 256)), 16)
     fused = al(part + B_ * (2 * K_ + 1) * 63 * 16, 256)
     assert L.spec_workspace_bytes(B_, K_, V_) == fused   # larger than the greedy chain's pruned layout here
-    fused1 = al(al(al(al(32 + 32, 32) + 1024 * 32 + 32, 16) + 4, 16) + 16, 256)
+    fused1 = al(al(al(al(32 + 32, 32) + 32, 16) + 4, 16) + 16, 256)
     assert L.spec_workspace_bytes(1, 0, 8) == max(fused1, al(256 + 64, 256))
     # tree: max(full sweep partials, pruned-kernel layout with at most ceil(V/4096) slices)
     nodes, smax = 128 * 64, -(-128256 // 4096)
