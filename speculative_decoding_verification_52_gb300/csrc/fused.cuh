@@ -426,17 +426,21 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
     row_bad = stt;
     if (!PROBS && row_bad == 0) row_bad = stq;
     if (!tok_bad && row_bad == 0) {
+      // accept iff q(x) == 0 or u < p(x)/q(x), with p(x) = ep / St and q(x) = eq / Sq:
+      // u * St * eq < ep * Sq, no division
       const double cd = static_cast<double>(a.c);
       const float zpf = in.zp, zqf = in.zq;
-      const double pa = exp2_d(static_cast<double>(zpf) * cd - static_cast<double>(At)) / St;
-      double qc;
+      const double ep = exp2_d(static_cast<double>(zpf) * cd - static_cast<double>(At));
+      double eq, Sqq;
       if (PROBS) {
         if (zqf != zqf || zqf < 0.f) row_bad = 1;
-        qc = static_cast<double>(zqf);
+        eq = static_cast<double>(zqf);
+        Sqq = 1.0;
       } else {
-        qc = exp2_d(static_cast<double>(zqf) * cd - static_cast<double>(Aq)) / Sq;
+        eq = exp2_d(static_cast<double>(zqf) * cd - static_cast<double>(Aq));
+        Sqq = Sq;
       }
-      acc_t = (qc == 0.0) || (static_cast<double>(u0) < pa / qc);
+      acc_t = (eq == 0.0) || (static_cast<double>(u0) * St * eq < ep * Sqq);
     }
   }
   const unsigned badtok = __ballot_sync(0xffffffffu, t < K && tok_bad);
@@ -475,8 +479,8 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
     inf.tstar = tstar;
     inf.AP = Ap;
     inf.AQ = has_q ? Aq2 : 0.f;
-    inf.iSp = static_cast<float>(1.0 / Sp);
-    inf.iSq = has_q ? static_cast<float>(1.0 / Sq2) : 1.f;
+    inf.iSp = __frcp_rn(static_cast<float>(Sp));   // scales of the residual weights: fp32 suffices
+    inf.iSq = has_q ? __frcp_rn(static_cast<float>(Sq2)) : 1.f;
     inf.u1 = a.uni[(static_cast<long long>(b) * W + tstar) * 2 + 1];
     inf.pad = 0.f;
     a.info[b] = inf;
@@ -625,12 +629,18 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
     const double lb = bb + (x2 - static_cast<double>(s));
     int cand = 0x7fffffff, lastpos = -1;
     if (s > 0.f && lb <= target && lb + static_cast<double>(s) > target) {
+      // the lane holding the target: search its 8 weights against the
+      // remaining mass (in fp32; the lane's own sum is exact enough here)
+      const float rem = static_cast<float>(target - lb);
       float run = 0.f;
+      int lastw = -1;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         run += w[i];
-        if (cand == 0x7fffffff && lb + static_cast<double>(run) > target) cand = e + i;
+        if (cand == 0x7fffffff && run > rem) cand = e + i;
+        if (w[i] > 0.f) lastw = e + i;
       }
+      if (cand == 0x7fffffff) cand = lastw;   // rounding at the lane's end: its last element with weight
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
