@@ -68,6 +68,10 @@ def lib() -> ctypes.CDLL:
             L.orc_residual_row.argtypes = [P, I, P, I, I, D, I, I, I, I, P, P]
             L.orc_residual_row.restype = I
             L.orc_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, I, P, P, P]
+            L.orc_tree_mask.argtypes = [P, I, I, P, P]
+            L.orc_tree_mask.restype = None
+            L.orc_kv_commit.argtypes = [P, P, P, P, P, I, I, I, I, ctypes.c_size_t, P]
+            L.orc_kv_commit.restype = None
             L.orc_verify_tree_greedy.restype = I
             _lib = L
     return _lib
@@ -211,3 +215,34 @@ def verify_tree_greedy(target, dtype, parents, node_tokens, max_depth: int):
     if rc:
         raise MemoryError("oracle allocation failed")
     return out, n, path
+
+
+def tree_mask(parents):
+    """Ancestor masks of per-sequence trees.  parents [B, N] (or [N] for one
+    tree); returns (masks [B, N, ceil(N/32)] uint32, status [B] int32)."""
+    par = np.atleast_2d(_c(parents, np.int32))
+    B, N = par.shape
+    NW = (N + 31) // 32
+    out = np.empty((B, N, NW), np.uint32)
+    st = np.empty(B, np.int32)
+    lib().orc_tree_mask(_ptr(par), B, N, _ptr(out), _ptr(st))
+    return out, st
+
+
+def kv_commit(cache, lengths, scratch, path, count):
+    """Append the selected scratch entries to the cache (a copy is returned).
+    cache [B, Lmax, ...], scratch [B, N, ...] (same trailing shape and dtype),
+    lengths [B], path [B, W] or None, count [B].  Returns (cache, new_lengths)."""
+    cache = np.array(cache, copy=True, order="C")
+    scratch = np.ascontiguousarray(scratch)
+    B, Lmax = cache.shape[:2]
+    N = scratch.shape[1]
+    E = cache[0, 0].nbytes if Lmax else scratch[0, 0].nbytes
+    ln = _c(lengths, np.int32)
+    cnt = _c(count, np.int32)
+    pth = None if path is None else _c(path, np.int32)
+    W = 0 if pth is None else pth.shape[1]
+    newl = np.empty(B, np.int32)
+    lib().orc_kv_commit(_ptr(cache), _ptr(ln), _ptr(scratch), None if pth is None else _ptr(pth), _ptr(cnt),
+                        B, Lmax, N, W, E, _ptr(newl))
+    return cache, newl

@@ -383,3 +383,67 @@ int orc_verify_tree_greedy(const void *target, int dtype, const int32_t *parents
   free(depth); free(acc); free(g); free(z);
   return 0;
 }
+
+/* Tree attention mask ([SDE] "Tree attention verification"; [SOTA] section 6):
+ * when the draft proposes a tree, the target checks every node in one pass
+ * with a causal mask that follows the tree instead of a line: a node sees only
+ * its ancestors (and itself).
+ *
+ * parents [B, N] (one tree per sequence; parents[b, 0] = -1 and
+ * 0 <= parents[b, i] < i), out [B, N, NW] uint32 with NW = ceil(N / 32):
+ * bit j % 32 of word j / 32 of row i is 1 iff node j is node i or one of its
+ * ancestors.  Computed by walking from i up to the root.  A sequence whose
+ * parents break the rule gets status -1 and an all-zero mask; status 0
+ * otherwise. */
+void orc_tree_mask(const int32_t *parents, int B, int N, uint32_t *out, int32_t *status) {
+  const int NW = (N + 31) / 32;
+  for (int b = 0; b < B; ++b) {
+    const int32_t *par = parents + (size_t)b * N;
+    uint32_t *mb = out + (size_t)b * N * NW;
+    for (size_t k = 0; k < (size_t)N * NW; ++k) mb[k] = 0u;
+    int ok = (N >= 1 && par[0] == -1);
+    for (int i = 1; ok && i < N; ++i)
+      if (par[i] < 0 || par[i] >= i) ok = 0;
+    status[b] = ok ? 0 : -1;
+    if (!ok) continue;
+    for (int i = 0; i < N; ++i) {
+      int node = i;
+      while (node >= 0) {
+        mb[(size_t)i * NW + node / 32] |= 1u << (node % 32);
+        node = par[node];
+      }
+    }
+  }
+}
+
+/* Commit on accept ([DVR] "KV rollback": verification writes the drafts'
+ * entries to a scratch buffer first and commits only what was accepted, so a
+ * rejection rolls the cache back to the accepted length).
+ *
+ * cache [B, Lmax, E] bytes, lengths [B], scratch [B, N, E] bytes, path [B, W]
+ * (the scratch slots to append, in order) or NULL for slots 0, 1, 2, ...,
+ * count [B] entries to append.  For each sequence: if count < 0 nothing is
+ * appended and new_lengths = lengths; if count > W (with a path), a slot is
+ * outside [0, N), or lengths + count > Lmax, nothing is appended and
+ * new_lengths = -1; otherwise entry j goes to position lengths + j and
+ * new_lengths = lengths + count.  Entries are copied byte for byte. */
+void orc_kv_commit(uint8_t *cache, const int32_t *lengths, const uint8_t *scratch, const int32_t *path,
+                   const int32_t *count, int B, int Lmax, int N, int W, size_t E, int32_t *new_lengths) {
+  for (int b = 0; b < B; ++b) {
+    const int n = count[b], L = lengths[b];
+    if (n < 0) { new_lengths[b] = L; continue; }
+    int ok = (L >= 0 && (long long)L + n <= Lmax && (path == NULL || n <= W));
+    for (int j = 0; ok && j < n; ++j) {
+      const int s = path ? path[(size_t)b * W + j] : j;
+      if (s < 0 || s >= N) ok = 0;
+    }
+    if (!ok) { new_lengths[b] = -1; continue; }
+    for (int j = 0; j < n; ++j) {
+      const int s = path ? path[(size_t)b * W + j] : j;
+      const uint8_t *src = scratch + ((size_t)b * N + (size_t)s) * E;
+      uint8_t *dst = cache + ((size_t)b * Lmax + (size_t)L + (size_t)j) * E;
+      for (size_t k = 0; k < E; ++k) dst[k] = src[k];
+    }
+    new_lengths[b] = L + n;
+  }
+}
