@@ -12,6 +12,8 @@ Other workloads (--workload):
           target row's argmax with probability 0.8
   tree    spec_verify_tree_greedy, B=128, N=64 nodes (BFS [4,3,2,1] truncated),
           V=128256, bf16; node tokens copy the parent's argmax with probability 0.7
+  treemask  spec_tree_mask, 4096 per-sequence trees of 256 nodes
+  kvcommit  spec_kv_commit, 256 chains, 64 KB entries
 Both read only the rows the greedy rules need (rows up to the first mismatch;
 accepted tree nodes), one persistent kernel per call; their algorithmic bytes
 are those rows, counted from the generator's own copy draws.
@@ -30,7 +32,7 @@ region, the SM clocks seen during the run, and the double-precision CPU
 oracle timed on a bounded sample on this host.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload sample|greedy|tree]
+                    [--workload sample|greedy|tree|treemask|kvcommit]
 """
 from __future__ import annotations
 
@@ -197,6 +199,8 @@ class Workload:
     kernel = ""
     per_rank = B
     launches_per_step = 1
+    dtype = "f32"            # what the path computes in
+    oracle_dtype = "f64"
 
     def describe(self) -> dict:
         raise NotImplementedError
@@ -393,7 +397,105 @@ class TreeWorkload(Workload):
         return hs, ds, step, [out, nacc, path]
 
 
-WORKLOADS = {w.name: w for w in (SampleWorkload(), GreedyWorkload(), TreeWorkload())}
+class TreeMaskWorkload(Workload):
+    name = "treemask"
+    metric = "tree-attention mask rows/s"
+    unit = "rows/s"
+    summary = "tree_mask_kernel_b4096_n256.md"
+    kernel = "tree_mask_kernel"
+    dtype = oracle_dtype = "u32"
+    per_rank = 4096
+    NODES = 256
+
+    def describe(self):
+        nw = (self.NODES + 31) // 32
+        return {"workload": "tree attention masks, B=4096 per-sequence trees of N=256 nodes (parent uniform over "
+                            "earlier nodes)", "B": self.per_rank, "N": self.NODES,
+                "input_bytes": 4 * self.per_rank * self.NODES,
+                "output_bytes": 4 * self.per_rank * self.NODES * nw,
+                "l2": "outputs (33.6 MB) within L2; steps are back to back"}
+
+    def batch(self, seqs):
+        from speculative_decoding_verification_52_gb300 import inputs as gen
+        par = gen.config_tree_masks(N=self.NODES, seqs=seqs)
+
+        class _B:
+            pass
+        b = _B()
+        b.B, b.N, b.parents = par.shape[0], par.shape[1], par
+        return b
+
+    def units(self, batch):
+        return batch.B * batch.N
+
+    def algorithmic_bytes(self, batch):
+        return 4 * batch.B * batch.N * (1 + (batch.N + 31) // 32) + 4 * batch.B
+
+    def oracle_call(self, batch, sl):
+        import oracle
+        oracle.tree_mask(batch.parents[sl])
+
+    def device_setup(self, batch, dev):
+        import torch
+
+        import speculative_decoding_verification_52_gb300 as sv
+        hs = [_pinned(batch.parents)]
+        ds = [h.to(dev) for h in hs]
+        masks = torch.empty((batch.B, batch.N, (batch.N + 31) // 32), dtype=torch.int32, device=dev)
+        status = torch.empty((batch.B,), dtype=torch.int32, device=dev)
+        stream = torch.cuda.current_stream()
+
+        def step():
+            sv.spec_tree_mask(ds[0], masks=masks, status=status, stream=stream)
+        return hs, ds, step, [masks, status]
+
+
+class KvCommitWorkload(Workload):
+    name = "kvcommit"
+    metric = "KV entries committed/s"
+    unit = "entries/s"
+    summary = "kv_commit_kernel_b256_e64k.md"
+    kernel = "kv_commit_kernel"
+    dtype = oracle_dtype = "u8"
+
+    def describe(self):
+        return {"workload": "KV commit-on-accept, B=256 chains of K=5 drafts (i.i.d. acceptance 0.75), 64 KB "
+                            "entries (32 layers x 8 KV heads x 128 x bf16), cache of 64 slots per sequence",
+                "B": B, "K": 5, "entry_bytes": 65536, "Lmax": 64,
+                "l2": "scratch (101 MB) and cache (1.07 GB) beyond L2 in total; steps re-commit the same entries",
+                "e2e_note": "the cache is resident state: end to end copies the scratch, lengths and counts"}
+
+    def batch(self, seqs):
+        from speculative_decoding_verification_52_gb300 import inputs as gen
+        return gen.config_kv_commit(seqs=seqs)
+
+    def units(self, batch):
+        return int(batch.count[batch.count > 0].sum())
+
+    def algorithmic_bytes(self, batch):
+        return 2 * self.units(batch) * batch.E + 12 * batch.B
+
+    def oracle_call(self, batch, sl):
+        import oracle
+        oracle.kv_commit(batch.cache[sl], batch.lengths[sl], batch.scratch[sl], None, batch.count[sl])
+
+    def device_setup(self, batch, dev):
+        import torch
+
+        import speculative_decoding_verification_52_gb300 as sv
+        hs = [_pinned(batch.scratch), _pinned(batch.lengths), _pinned(batch.count)]
+        ds = [h.to(dev) for h in hs]
+        cache = torch.from_numpy(batch.cache).to(dev)
+        newl = torch.empty((batch.B,), dtype=torch.int32, device=dev)
+        stream = torch.cuda.current_stream()
+
+        def step():
+            sv.spec_kv_commit(cache, ds[1], ds[0], ds[2], new_lengths=newl, stream=stream)
+        return hs, ds, step, [newl]
+
+
+WORKLOADS = {w.name: w for w in (SampleWorkload(), GreedyWorkload(), TreeWorkload(), TreeMaskWorkload(),
+                                 KvCommitWorkload())}
 
 
 def oracle_rate(wl: Workload, batch, budget_s: float, min_seqs: int):
@@ -430,7 +532,7 @@ def run_reference(args, wl: Workload, ws, rank):
     sample = f"{per_step} of the {wl.per_rank} sequences per step"
     line = {"impl": "reference", "metric": wl.metric, "value": value, "unit": wl.unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.oracle_dtype,
             "data": "synthetic", "config": wl.describe(),
             "cpu_baseline": {"value": value, "unit": wl.unit, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -537,7 +639,7 @@ def run_ours(args, wl: Workload, ws, rank, local):
     line = {
         "metric": wl.metric, "value": ws * units / (ms * 1e-3), "unit": wl.unit, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic", "config": cfg, "roofline": roof,
+        "dtype": wl.dtype, "data": "synthetic", "config": cfg, "roofline": roof,
         "e2e": {"value": ws * units / (e2e_ms * 1e-3), "unit": wl.unit,
                 "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in hs),
                 "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in houts), "ms_per_step": e2e_ms},

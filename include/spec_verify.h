@@ -183,6 +183,46 @@ spec_status_t spec_debug_residual(const void *target_logits, spec_dtype_t target
                                   int32_t *out_tokens, int32_t *num_accepted, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
+/* Tree attention mask ("Speculative decoding and EAGLE", section "Tree
+ * attention verification"; "Speculative Decoding: from idea to SOTA",
+ * section 6): when the draft proposes a tree, the target scores all of it in
+ * one pass under a mask in which every node attends only to its ancestors and
+ * itself.
+ *
+ *   parents [B, N] int32 (device): one tree per sequence, parents[b, 0] = -1
+ *       and 0 <= parents[b, i] < i (breadth-first or any topological order).
+ *   masks [B, N, ceil(N/32)] uint32 (device, written): bit j % 32 of word
+ *       j / 32 of row i is set iff node j is node i or one of its ancestors.
+ *   status [B] int32 (device, written): 0, or -1 when the sequence's parents
+ *       break the rule above (its mask is then all zero).
+ *
+ * Limits: 1 <= N <= 1024. */
+spec_status_t spec_tree_mask(const int32_t *parents, int B, int N, uint32_t *masks, int32_t *status,
+                             void *stream);
+
+/* Commit on accept for the KV cache ("Speculative decoding: draft, verify,
+ * repeat", KV rollback): the verification pass writes the drafts' entries to a
+ * scratch buffer; only the accepted ones are appended to the cache, so a
+ * rejection leaves the cache at the accepted length.
+ *
+ *   cache [B, Lmax, entry_bytes] (device, appended to in place).
+ *   lengths [B] int32 (device): the cache lengths before the call.
+ *   scratch [B, N, entry_bytes] (device): the entries of the verified positions.
+ *   path [B, W] int32 (device) or NULL: the scratch slots to append, in order
+ *       (e.g. out_path of spec_verify_tree_greedy); NULL means slots 0, 1, ...
+ *       (a chain: the first num_accepted drafts).
+ *   count [B] int32 (device): entries to append (e.g. num_accepted); a
+ *       negative count appends nothing.
+ *   new_lengths [B] int32 (device, written): lengths + count; lengths when
+ *       count < 0; -1 (nothing appended) when the append would pass Lmax, a
+ *       slot is outside [0, N) or count > W with a path.
+ *
+ * Entries are opaque bytes (call once for keys and once for values, or lay
+ * them out together).  new_lengths must not alias lengths. */
+spec_status_t spec_kv_commit(void *cache, const int32_t *lengths, const void *scratch, const int32_t *path,
+                             const int32_t *count, int B, int Lmax, int N, int W, size_t entry_bytes,
+                             int32_t *new_lengths, void *stream);
+
 /* Timing hooks for benchmarks: while enabled, each verify call records CUDA
  * events on the call's stream around its kernels (at most max_calls calls are
  * recorded).  spec_profile_end synchronises on the recorded events and returns

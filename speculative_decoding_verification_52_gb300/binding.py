@@ -61,6 +61,10 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_tree_greedy.restype = I
             L.spec_debug_residual.argtypes = [P, I, P, I, I, P, P, F, I, I, I, I, I, P, P, P, P, P, Z, P]
             L.spec_debug_residual.restype = I
+            L.spec_tree_mask.argtypes = [P, I, I, P, P, P]
+            L.spec_tree_mask.restype = I
+            L.spec_kv_commit.argtypes = [P, P, P, P, P, I, I, I, I, Z, P, P]
+            L.spec_kv_commit.restype = I
             L.spec_profile_begin.argtypes = [I]
             L.spec_profile_begin.restype = I
             L.spec_profile_end.argtypes = [P, P, P]
@@ -247,6 +251,44 @@ def spec_debug_residual(target_logits, draft, draft_tokens, uniforms, temperatur
                                    _ptr(ws), ws.numel(), _stream(stream))
     _check("spec_debug_residual", st)
     return row, mass, out_tokens, num_accepted
+
+
+def spec_tree_mask(parents, *, masks=None, status=None, stream=None):
+    """Ancestor masks.  parents [B, N] (or [N]) int32 on the device.  Returns
+    (masks [B, N, ceil(N/32)] int32 holding the uint32 bit words, status [B])."""
+    _dev(parents, "parents")
+    par = parents if parents.dim() == 2 else parents.unsqueeze(0)
+    par = par.contiguous()
+    B, N = par.shape
+    NW = (N + 31) // 32
+    if masks is None:
+        masks = torch.empty((B, N, NW), dtype=torch.int32, device=par.device)
+    if status is None:
+        status = torch.empty((B,), dtype=torch.int32, device=par.device)
+    st = lib().spec_tree_mask(_ptr(par), B, N, _ptr(masks), _ptr(status), _stream(stream))
+    _check("spec_tree_mask", st)
+    return masks, status
+
+
+def spec_kv_commit(cache, lengths, scratch, count, *, path=None, new_lengths=None, stream=None):
+    """Append the selected scratch entries to the cache in place.  cache
+    [B, Lmax, ...], scratch [B, N, ...] (same trailing shape and dtype),
+    lengths / count [B] int32, path [B, W] int32 or None.  Returns new_lengths."""
+    for t, n in ((cache, "cache"), (lengths, "lengths"), (scratch, "scratch"), (count, "count")):
+        _dev(t, n)
+    B, Lmax = cache.shape[:2]
+    N = scratch.shape[1]
+    E = cache[0, 0].numel() * cache.element_size() if Lmax else scratch[0, 0].numel() * scratch.element_size()
+    W = 0
+    if path is not None:
+        _dev(path, "path")
+        W = path.shape[1]
+    if new_lengths is None:
+        new_lengths = torch.empty((B,), dtype=torch.int32, device=cache.device)
+    st = lib().spec_kv_commit(_ptr(cache), _ptr(lengths), _ptr(scratch), _ptr(path), _ptr(count), B, Lmax, N, W, E,
+                              _ptr(new_lengths), _stream(stream))
+    _check("spec_kv_commit", st)
+    return new_lengths
 
 
 def spec_profile_begin(max_calls: int):

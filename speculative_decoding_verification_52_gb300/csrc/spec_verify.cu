@@ -25,6 +25,8 @@
 #include "spec_verify.h"
 #include "sweep.cuh"
 #include "tree.cuh"
+#include "tree_mask.cuh"
+#include "kv_commit.cuh"
 
 namespace {
 
@@ -816,6 +818,73 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t ta
     finish_tree_kernel<<<B, FT_THREADS, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "tree finish launch");
+    prof_mark(2, st);
+    return SPEC_OK;
+  } catch (...) {
+    return fail(SPEC_ERR_CUDA, "unexpected host exception");
+  }
+}
+
+spec_status_t spec_tree_mask(const int32_t* parents, int B, int N, uint32_t* masks, int32_t* status, void* stream) {
+  try {
+    if (B < 0) return fail(SPEC_ERR_INVALID_ARG, "B=%d must be >= 0", B);
+    if (N < 1 || N > TM_MAX_N) return fail(SPEC_ERR_INVALID_ARG, "N=%d outside [1, %d]", N, TM_MAX_N);
+    if (B == 0) return SPEC_OK;
+    if (!parents || !masks || !status) return fail(SPEC_ERR_INVALID_ARG, "NULL parents/masks/status");
+    int dev;
+    DevInfo di;
+    spec_status_t s = device_info(di, dev);
+    if (s != SPEC_OK) return s;
+    const size_t smem = sizeof(int) * static_cast<size_t>(N) + sizeof(uint32_t) * TM_THREADS * ((N + 31) / 32);
+    const int grid = std::min(B, di.sms * 8);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    prof_mark(0, st);
+    tree_mask_kernel<<<grid, TM_THREADS, smem, st>>>(parents, B, N, masks, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "tree mask launch");
+    prof_mark(1, st);
+    prof_mark(2, st);
+    return SPEC_OK;
+  } catch (...) {
+    return fail(SPEC_ERR_CUDA, "unexpected host exception");
+  }
+}
+
+spec_status_t spec_kv_commit(void* cache, const int32_t* lengths, const void* scratch, const int32_t* path,
+                             const int32_t* count, int B, int Lmax, int N, int W, size_t entry_bytes,
+                             int32_t* new_lengths, void* stream) {
+  try {
+    if (B < 0 || Lmax < 0 || N < 1 || entry_bytes < 1 || (path && W < 1))
+      return fail(SPEC_ERR_INVALID_ARG, "bad sizes B=%d Lmax=%d N=%d W=%d entry_bytes=%zu", B, Lmax, N, W, entry_bytes);
+    if (B == 0) return SPEC_OK;
+    if (!cache || !lengths || !scratch || !count || !new_lengths)
+      return fail(SPEC_ERR_INVALID_ARG, "NULL cache/lengths/scratch/count/new_lengths");
+    int dev;
+    DevInfo di;
+    spec_status_t s = device_info(di, dev);
+    if (s != SPEC_OK) return s;
+    KvCommitArgs a{};
+    a.cache = static_cast<unsigned char*>(cache);
+    a.lengths = lengths;
+    a.scratch = static_cast<const unsigned char*>(scratch);
+    a.path = path;
+    a.count = count;
+    a.B = B;
+    a.Lmax = Lmax;
+    a.N = N;
+    a.W = path ? W : 0;
+    a.J = path ? W : N;
+    a.E = entry_bytes;
+    a.new_lengths = new_lengths;
+    a.vec = entry_bytes % 16 == 0 && aligned16(cache) && aligned16(scratch);
+    const long long pairs = static_cast<long long>(B) * a.J;
+    const int grid = static_cast<int>(std::min<long long>(pairs, static_cast<long long>(di.sms) * 16));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    prof_mark(0, st);
+    kv_commit_kernel<<<grid, KV_THREADS, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kv commit launch");
+    prof_mark(1, st);
     prof_mark(2, st);
     return SPEC_OK;
   } catch (...) {

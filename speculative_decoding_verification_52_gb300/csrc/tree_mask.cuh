@@ -1,0 +1,51 @@
+// tree_mask.cuh -- the tree attention mask: every node of a candidate tree
+// attends only to its ancestors and itself ("Speculative decoding and EAGLE",
+// section "Tree attention verification"; "Speculative Decoding: from idea to
+// SOTA", section 6).
+//
+// One CTA per sequence (grid-stride over sequences): the sequence's parent
+// array is staged in shared memory and checked (parents[0] = -1,
+// 0 <= parents[i] < i); then each thread builds the masks of its rows, one at a
+// time, in a private shared-memory row of NW = ceil(N/32) words by walking from
+// the node up to the root, and writes the row out (the rows of consecutive
+// threads are consecutive in memory, so the stores coalesce).
+#pragma once
+
+#include "common.cuh"
+
+namespace sv {
+
+constexpr int TM_THREADS = 128;
+constexpr int TM_MAX_N = 1024;
+
+__global__ void __launch_bounds__(TM_THREADS) tree_mask_kernel(const int32_t* __restrict__ parents, int B, int N,
+                                                               uint32_t* __restrict__ out, int32_t* __restrict__ status) {
+  extern __shared__ __align__(16) unsigned char tm_smem[];
+  const int NW = (N + 31) / 32;
+  int* par = reinterpret_cast<int*>(tm_smem);
+  uint32_t* rowbuf = reinterpret_cast<uint32_t*>(par + N) + threadIdx.x * NW;
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    const int32_t* pb = parents + static_cast<long long>(b) * N;
+    bool ok = true;
+    for (int i = threadIdx.x; i < N; i += TM_THREADS) {
+      const int p = pb[i];
+      par[i] = p;
+      ok &= (i == 0) ? (p == -1) : (p >= 0 && p < i);
+    }
+    ok = __syncthreads_and(ok);
+    uint32_t* ob = out + static_cast<long long>(b) * N * NW;
+    for (int i = threadIdx.x; i < N; i += TM_THREADS) {
+      for (int w = 0; w < NW; ++w) rowbuf[w] = 0u;
+      if (ok) {
+        // parents[node] < node on a valid tree, so the walk ends at the root
+        for (int node = i; node >= 0; node = par[node]) rowbuf[node >> 5] |= 1u << (node & 31);
+      }
+      uint32_t* orow = ob + static_cast<long long>(i) * NW;
+      for (int w = 0; w < NW; ++w) orow[w] = rowbuf[w];
+    }
+    if (threadIdx.x == 0) status[b] = ok ? 0 : -1;
+    __syncthreads();   // par is reused by the next sequence
+  }
+}
+
+}  // namespace sv

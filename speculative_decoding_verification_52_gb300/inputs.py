@@ -252,6 +252,58 @@ def config_greedy(B: int = 256, V: int = 128256, K: int = 5, match_prob: float =
                       meta=dict(copied=copied, match_prob=match_prob, seed=seed, seqs=seqs))
 
 
+def config_tree_masks(B: int = 4096, N: int = 256, seed: int = 52_700, seqs=None) -> np.ndarray:
+    """Per-sequence candidate trees (a dynamic tree per sequence, as a drafter
+    that widens where it is unsure would build): node i's parent is uniform
+    over the nodes before it.  Returns parents [B, N] int32, parents[:, 0] = -1."""
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    par = np.empty((len(seqs), N), dtype=np.int32)
+    for i, b in enumerate(seqs):
+        rng = _rng(seed, b)
+        par[i, 0] = -1
+        if N > 1:
+            par[i, 1:] = np.floor(rng.random(N - 1) * np.arange(1, N)).astype(np.int32)
+    return par
+
+
+@dataclass
+class KvBatch:
+    """Inputs of one KV commit: cache [B, Lmax, E] bytes, lengths [B],
+    scratch [B, N, E] bytes, count [B] (entries to append, slots 0..count-1)."""
+
+    B: int
+    Lmax: int
+    N: int
+    E: int
+    cache: np.ndarray
+    lengths: np.ndarray
+    scratch: np.ndarray
+    count: np.ndarray
+
+
+def config_kv_commit(B: int = 256, K: int = 5, E: int = 65536, Lmax: int = 64, alpha: float = 0.75,
+                     seed: int = 52_800, seqs=None) -> KvBatch:
+    """Chain drafts of length K with i.i.d. acceptance alpha: the number of
+    accepted drafts is the run of successes before the first failure (capped
+    at K).  Entries are E random bytes (e.g. 32 layers x 8 KV heads x 128 dims
+    x bf16 = 64 KB per token); the scratch buffer holds K + 1 slots."""
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    n = len(seqs)
+    N = K + 1
+    cache = np.empty((n, Lmax, E), dtype=np.uint8)
+    scratch = np.empty((n, N, E), dtype=np.uint8)
+    lengths = np.empty(n, dtype=np.int32)
+    count = np.empty(n, dtype=np.int32)
+    for i, b in enumerate(seqs):
+        rng = _rng(seed, b)
+        cache[i] = rng.integers(0, 256, size=(Lmax, E), dtype=np.uint8)
+        scratch[i] = rng.integers(0, 256, size=(N, E), dtype=np.uint8)
+        lengths[i] = int(rng.integers(0, Lmax - K))
+        runs = rng.random(K) < alpha
+        count[i] = K if runs.all() else int(np.argmin(runs))
+    return KvBatch(n, Lmax, N, E, cache, lengths, scratch, count)
+
+
 def bfs_tree(branching, max_nodes=None) -> np.ndarray:
     """Parent array of a static tree in breadth-first order: the root, then
     ``branching[0]`` children of the root, then ``branching[1]`` children of
@@ -310,5 +362,5 @@ __all__ = [
     "F32", "BF16", "ChainBatch", "TreeBatch", "SIGMA_B256_V128K", "config_greedy",
     "f32_to_bf16_bits", "bf16_bits_to_f64", "as_f64", "gaussian_chain",
     "config_tiny", "config_zipf", "config_headline", "config_controlled",
-    "config_tree", "bfs_tree", "tree_depths",
+    "config_tree", "bfs_tree", "tree_depths", "config_tree_masks", "KvBatch", "config_kv_commit",
 ]

@@ -111,3 +111,17 @@ def test_status_strings(L):
     assert B.status_string(0) == "SPEC_OK"
     assert B.status_string(4) == "SPEC_ERR_WORKSPACE"
     assert B.status_string(99) == "SPEC_ERR_UNKNOWN"
+
+
+def test_tree_mask_and_kv_commit_reject_bad_arguments(L):
+    P = ctypes.c_void_p
+    assert L.spec_tree_mask(P(16), 2, 0, P(32), P(48), None) == B.SPEC_ERR_INVALID_ARG
+    assert L.spec_tree_mask(P(16), 2, 1025, P(32), P(48), None) == B.SPEC_ERR_INVALID_ARG
+    assert L.spec_tree_mask(None, 2, 8, P(32), P(48), None) == B.SPEC_ERR_INVALID_ARG
+    assert L.spec_tree_mask(None, 0, 8, None, None, None) == B.SPEC_OK
+    kv = L.spec_kv_commit
+    assert kv(P(16), P(32), P(48), None, P(64), 2, 8, 0, 0, 64, P(80), None) == B.SPEC_ERR_INVALID_ARG
+    assert kv(P(16), P(32), P(48), P(96), P(64), 2, 8, 4, 0, 64, P(80), None) == B.SPEC_ERR_INVALID_ARG
+    assert kv(P(16), P(32), P(48), None, P(64), 2, 8, 4, 0, 0, P(80), None) == B.SPEC_ERR_INVALID_ARG
+    assert kv(P(16), None, P(48), None, P(64), 2, 8, 4, 0, 64, P(80), None) == B.SPEC_ERR_INVALID_ARG
+    assert kv(None, None, None, None, None, 0, 8, 4, 0, 64, None, None) == B.SPEC_OK
