@@ -48,4 +48,55 @@ __global__ void __launch_bounds__(TM_THREADS) tree_mask_kernel(const int32_t* __
   }
 }
 
+// The same walk with the row held in registers (up to NWT words, a
+// compile-time count, so every word access is a register select) and written
+// with vector stores when the row is exactly NWT words: one thread per row, the
+// sequence's parents in shared memory.
+template <int NWT>
+__global__ void __launch_bounds__(TM_THREADS) tree_mask_reg_kernel(const int32_t* __restrict__ parents, int B, int N,
+                                                                   uint32_t* __restrict__ out,
+                                                                   int32_t* __restrict__ status) {
+  extern __shared__ __align__(16) unsigned char tm_smem[];
+  int* par = reinterpret_cast<int*>(tm_smem);
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    const int32_t* pb = parents + static_cast<long long>(b) * N;
+    bool ok = true;
+    for (int i = threadIdx.x; i < N; i += TM_THREADS) {
+      const int p = pb[i];
+      par[i] = p;
+      ok &= (i == 0) ? (p == -1) : (p >= 0 && p < i);
+    }
+    ok = __syncthreads_and(ok);
+    const int NW = (N + 31) / 32;   // the row stride; NW <= NWT
+    uint32_t* ob = out + static_cast<long long>(b) * N * NW;
+    for (int i = threadIdx.x; i < N; i += TM_THREADS) {
+      uint32_t row[NWT];
+#pragma unroll
+      for (int w = 0; w < NWT; ++w) row[w] = 0u;
+      if (ok) {
+        for (int node = i; node >= 0; node = par[node]) {
+          const int wn = node >> 5;
+          const uint32_t bit = 1u << (node & 31);
+#pragma unroll
+          for (int w = 0; w < NWT; ++w) row[w] |= (w == wn) ? bit : 0u;
+        }
+      }
+      uint32_t* orow = ob + static_cast<long long>(i) * NW;
+      if (NW == NWT && NWT % 4 == 0) {
+#pragma unroll
+        for (int w = 0; w < NWT; w += 4)
+          reinterpret_cast<uint4*>(orow)[w / 4] = make_uint4(row[w], row[w + 1], row[w + 2], row[w + 3]);
+      } else if (NW == NWT && NWT == 2) {
+        reinterpret_cast<uint2*>(orow)[0] = make_uint2(row[0], row[NWT - 1]);
+      } else {
+#pragma unroll
+        for (int w = 0; w < NWT; ++w)
+          if (w < NW) orow[w] = row[w];
+      }
+    }
+    if (threadIdx.x == 0) status[b] = ok ? 0 : -1;
+    __syncthreads();   // par is reused by the next sequence
+  }
+}
+
 }  // namespace sv

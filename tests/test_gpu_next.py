@@ -26,7 +26,7 @@ def test_tree_mask_page_example_and_static_trees(orc):
         np.testing.assert_array_equal(m, rm)
 
 
-@pytest.mark.parametrize("N", [2, 31, 32, 33, 100, 257])
+@pytest.mark.parametrize("N", [2, 31, 32, 33, 70, 100, 257, 500, 600])
 def test_tree_mask_random_per_sequence_trees(orc, N):
     rng = np.random.default_rng(N)
     B = 37
