@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L.orc_tree_mask.restype = None
             L.orc_kv_commit.argtypes = [P, P, P, P, P, I, I, I, I, ctypes.c_size_t, P]
             L.orc_kv_commit.restype = None
+            L.orc_row_stats.argtypes = [P, I, P, I, I, D, I, I, I, P, P, P]
+            L.orc_row_stats.restype = I
             L.orc_verify_tree_greedy.restype = I
             _lib = L
     return _lib
@@ -246,3 +248,17 @@ def kv_commit(cache, lengths, scratch, path, count):
     lib().orc_kv_commit(_ptr(cache), _ptr(ln), _ptr(scratch), None if pth is None else _ptr(pth), _ptr(cnt),
                         B, Lmax, N, W, E, _ptr(newl))
     return cache, newl
+
+
+def row_stats(target, target_dtype, draft, draft_dtype, draft_is_probs, T: float):
+    """Per drafted position: (alpha = sum min(p, q), KL(q || p), TV), each [B, K]."""
+    t = _raw(target, target_dtype)
+    B, W, V = t.shape
+    K = W - 1
+    d = _raw(draft, "f32" if draft_is_probs else draft_dtype)
+    out = [np.empty((B, K), np.float64) for _ in range(3)]
+    rc = lib().orc_row_stats(_ptr(t), _dt(target_dtype), _ptr(d), _dt("f32" if draft_is_probs else draft_dtype),
+                             1 if draft_is_probs else 0, float(T), B, K, V, *[_ptr(o) for o in out])
+    if rc:
+        raise MemoryError("oracle allocation failed")
+    return tuple(out)

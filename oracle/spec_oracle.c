@@ -447,3 +447,53 @@ void orc_kv_commit(uint8_t *cache, const int32_t *lengths, const uint8_t *scratc
     new_lengths[b] = L + n;
   }
 }
+
+/* Acceptance statistics of a draft against its target, per drafted position
+ * ([DVR] step 4: acceptance rate against the divergence between draft and
+ * verifier; [SOTA] section 3: a draft token is accepted with probability
+ * min(1, p/q), so position t is accepted with probability
+ * alpha_t = sum_v min(p_t(v), q_t(v))).
+ *
+ * For t = 0..K-1 of each sequence, with p_t = softmax(target[b,t]/T) and q_t
+ * the draft distribution (softmax(draft[b,t]/T), or the given probabilities):
+ *   alpha[b,t] = sum_v min(p, q)
+ *   kl[b,t]    = KL(q || p) = sum_{v: q > 0} q log(q / p)   (+inf if some p = 0 < q)
+ *   tv[b,t]    = 1/2 sum_v |p - q|
+ * Rows that are invalid (NaN, +inf, no finite entry; NaN or negative
+ * probabilities) give NaN in all three. */
+int orc_row_stats(const void *target, int target_dtype, const void *draft, int draft_dtype, int draft_is_probs,
+                  double T, int B, int K, int V, double *alpha, double *kl, double *tv) {
+  const int W = K + 1;
+  double *z = (double *)malloc(sizeof(double) * (size_t)V);
+  double *p = (double *)malloc(sizeof(double) * (size_t)V);
+  double *q = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!z || !p || !q) { free(z); free(p); free(q); return 2; }
+  for (int b = 0; b < B; ++b) {
+    for (int t = 0; t < K; ++t) {
+      const size_t o = (size_t)b * K + t;
+      int bad = 0;
+      orc_widen_row(target, target_dtype, ((size_t)b * W + t) * (size_t)V, V, z);
+      if (orc_softmax(z, V, T, p)) bad = 1;
+      if (draft_is_probs) {
+        orc_widen_row(draft, ORC_F32, o * (size_t)V, V, q);
+        for (int v = 0; v < V; ++v)
+          if (isnan(q[v]) || q[v] < 0.0) bad = 1;
+      } else {
+        orc_widen_row(draft, draft_dtype, o * (size_t)V, V, z);
+        if (orc_softmax(z, V, T, q)) bad = 1;
+      }
+      if (bad) { alpha[o] = kl[o] = tv[o] = NAN; continue; }
+      double a = 0.0, k = 0.0, d = 0.0;
+      for (int v = 0; v < V; ++v) {
+        a += (p[v] < q[v]) ? p[v] : q[v];
+        d += fabs(p[v] - q[v]);
+        if (q[v] > 0.0) k += (p[v] > 0.0) ? q[v] * log(q[v] / p[v]) : INFINITY;
+      }
+      alpha[o] = a;
+      kl[o] = k;
+      tv[o] = 0.5 * d;
+    }
+  }
+  free(z); free(p); free(q);
+  return 0;
+}

@@ -99,3 +99,71 @@ def test_kv_commit_paths_and_errors(orc):
     o1, n1 = orc.kv_commit(cache, lengths, scratch, np.tile(np.arange(W), (B, 1)), [2, 2, 1, -1])
     o2, n2 = orc.kv_commit(cache, lengths, scratch, None, [2, 2, 1, -1])
     assert (o1 == o2).all() and (n1 == n2).all() and n2[3] == lengths[3]
+
+
+# --- acceptance statistics ------------------------------------------------------
+
+def _stats_batch(rng, B, K, V, scale=2.0, sigma=0.7):
+    z = scale * rng.standard_normal((B, K + 1, V))
+    y = z[:, :K] + sigma * rng.standard_normal((B, K, V))
+    return z.astype(np.float32), y.astype(np.float32)
+
+
+def test_row_stats_match_scipy(orc):
+    from scipy.special import rel_entr, softmax
+    rng = np.random.default_rng(9)
+    z, y = _stats_batch(rng, 3, 4, 500)
+    T = 0.8
+    a, k, tv = orc.row_stats(z, "f32", y, "f32", False, T)
+    P = softmax(z[:, :4].astype(np.float64) / T, axis=-1)
+    Q = softmax(y.astype(np.float64) / T, axis=-1)
+    np.testing.assert_allclose(a, np.minimum(P, Q).sum(-1), rtol=1e-12)
+    np.testing.assert_allclose(k, rel_entr(Q, P).sum(-1), rtol=1e-10)
+    np.testing.assert_allclose(tv, 0.5 * np.abs(P - Q).sum(-1), rtol=1e-12)
+
+
+def test_row_stats_identities(orc):
+    rng = np.random.default_rng(10)
+    for sigma in (0.01, 0.3, 1.0, 3.0):
+        z, y = _stats_batch(rng, 2, 3, 1000, sigma=sigma)
+        a, k, tv = orc.row_stats(z, "f32", y, "f32", False, 1.0)
+        np.testing.assert_allclose(tv, 1.0 - a, atol=1e-12)     # TV = 1 - sum min(p, q)
+        assert (tv <= np.sqrt(k / 2.0) + 1e-12).all()           # Pinsker
+        assert (k >= 0).all() and ((0 <= a) & (a <= 1)).all()
+    z, _ = _stats_batch(rng, 2, 3, 300)
+    a, k, tv = orc.row_stats(z, "f32", z[:, :3], "f32", False, 0.7)   # q = p
+    np.testing.assert_allclose(a, 1.0, atol=1e-12)
+    np.testing.assert_allclose(k, 0.0, atol=1e-12)
+
+
+def test_row_stats_two_point_closed_form(orc):
+    for pa, qa in [(0.3, 0.6), (0.9, 0.1), (0.5, 0.5)]:
+        z = np.log(np.array([[[pa, 1 - pa], [0.5, 0.5]]]))
+        y = np.array([[[qa, 1 - qa]]], np.float32)
+        a, k, tv = orc.row_stats(z.astype(np.float32), "f32", y, "f32", True, 1.0)
+        assert a[0, 0] == pytest.approx(min(pa, qa) + min(1 - pa, 1 - qa), abs=1e-7)
+        assert k[0, 0] == pytest.approx(qa * np.log(qa / pa) + (1 - qa) * np.log((1 - qa) / (1 - pa)), abs=1e-6)
+
+
+def test_alpha_is_the_acceptance_probability_of_the_law(orc):
+    """alpha_0 is the probability that position 0 is accepted, by the
+    brute-force law of one verification step (every draft, every branch)."""
+    from scipy.special import softmax
+    from test_oracle_law import exact_law
+    rng = np.random.default_rng(11)
+    for V in (3, 5, 8):
+        z, y = _stats_batch(rng, 1, 2, V, scale=1.0, sigma=0.8)
+        a, _, _ = orc.row_stats(z, "f32", y, "f32", False, 1.0)
+        law = exact_law(softmax(z[0].astype(np.float64), axis=-1), softmax(y[0].astype(np.float64), axis=-1))
+        p_acc0 = sum(pr for (n, _), pr in law.items() if n >= 1)
+        assert a[0, 0] == pytest.approx(p_acc0, abs=1e-12)
+
+
+def test_row_stats_invalid_rows(orc):
+    rng = np.random.default_rng(12)
+    z, y = _stats_batch(rng, 2, 2, 50)
+    z[0, 1, 3] = np.nan
+    y[1, 0, 7] = np.inf
+    a, k, tv = orc.row_stats(z, "f32", y, "f32", False, 1.0)
+    assert np.isnan(a[0, 1]) and np.isnan(k[1, 0]) and np.isnan(tv[1, 0])
+    assert np.isfinite(a[0, 0]) and np.isfinite(a[1, 1])
