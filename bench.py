@@ -14,6 +14,7 @@ Other workloads (--workload):
           V=128256, bf16; node tokens copy the parent's argmax with probability 0.7
   treemask  spec_tree_mask, 4096 per-sequence trees of 256 nodes
   kvcommit  spec_kv_commit, 256 chains, 64 KB entries
+  stats     spec_row_stats over the default workload's rows: sum min(p,q), KL, TV
 Both read only the rows the greedy rules need (rows up to the first mismatch;
 accepted tree nodes), one persistent kernel per call; their algorithmic bytes
 are those rows, counted from the generator's own copy draws.
@@ -32,7 +33,7 @@ region, the SM clocks seen during the run, and the double-precision CPU
 oracle timed on a bounded sample on this host.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload sample|greedy|tree|treemask|kvcommit]
+                    [--workload sample|greedy|tree|treemask|kvcommit|stats]
 """
 from __future__ import annotations
 
@@ -68,17 +69,20 @@ def metric_bytes(b=B, k=K, v=V, elem=2):
     return (b * (k + 1) * v + b * k * v + b * v) * elem
 
 
-def source_sha() -> str:
+def source_sha(files=None) -> str:
+    """Hash of the kernel sources a profile was taken on: the given csrc files
+    (the kernel's own header plus the shared helpers), or all of csrc."""
     d = os.path.join(ROOT, "speculative_decoding_verification_52_gb300", "csrc")
+    names = sorted(files) if files else sorted(os.listdir(d))
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
+    for f in names:
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(summary: str):
+def profiled_traffic(summary: str, files=None):
     """dram read+write bytes per launch of the dominant kernel from a committed
     ncu summary, only if it was taken on the current kernel sources."""
     try:
@@ -88,7 +92,7 @@ def profiled_traffic(summary: str):
                 if ":" in line:
                     k_, v_ = line.split(":", 1)
                     kv[k_.strip()] = v_.strip()
-        if kv.get("source_sha") != source_sha():
+        if kv.get("source_sha") != source_sha(files):
             return None
         return int(float(kv["dram_bytes_per_launch"]))
     except (OSError, KeyError, ValueError):
@@ -197,6 +201,7 @@ class Workload:
     unit = UNIT
     summary = ""
     kernel = ""
+    sources = ()             # csrc files the dominant kernel is built from
     per_rank = B
     launches_per_step = 1
     dtype = "f32"            # what the path computes in
@@ -242,6 +247,7 @@ class SampleWorkload(Workload):
     name = "sample"
     summary = "fused_sample_kernel_b256_v128256_k5_bf16.md"
     kernel = "fused_sample_kernel<bf16 target, bf16 draft logits>"
+    sources = ("common.cuh", "fused.cuh")
 
     def describe(self):
         return {"workload": "spec-verify sampling B=256 V=128256 K=5 bf16 T=0.7 (target+draft logits, accept scan, "
@@ -296,6 +302,7 @@ class GreedyWorkload(Workload):
     name = "greedy"
     summary = "tree_greedy_kernel_chain_b256_v128256_k5_bf16.md"
     kernel = "tree_greedy_kernel<bf16> (chain mode)"
+    sources = ("common.cuh", "tree.cuh")
 
     def describe(self):
         return {"workload": "spec-verify greedy B=256 V=128256 K=5 bf16, draft = target argmax w.p. 0.8 "
@@ -342,6 +349,7 @@ class TreeWorkload(Workload):
     unit = "nodes/s"
     summary = "tree_greedy_kernel_b128_n64_v128256_bf16.md"
     kernel = "tree_greedy_kernel<bf16>"
+    sources = ("common.cuh", "tree.cuh")
     per_rank = TREE_B
 
     def describe(self):
@@ -402,7 +410,8 @@ class TreeMaskWorkload(Workload):
     metric = "tree-attention mask rows/s"
     unit = "rows/s"
     summary = "tree_mask_kernel_b4096_n256.md"
-    kernel = "tree_mask_kernel"
+    kernel = "tree_mask_reg_kernel<8>"
+    sources = ("tree_mask.cuh",)
     dtype = oracle_dtype = "u32"
     per_rank = 4096
     NODES = 256
@@ -456,6 +465,7 @@ class KvCommitWorkload(Workload):
     unit = "entries/s"
     summary = "kv_commit_kernel_b256_e64k.md"
     kernel = "kv_commit_kernel"
+    sources = ("kv_commit.cuh",)
     dtype = oracle_dtype = "u8"
 
     def describe(self):
@@ -494,8 +504,51 @@ class KvCommitWorkload(Workload):
         return hs, ds, step, [newl]
 
 
+class StatsWorkload(Workload):
+    name = "stats"
+    metric = "draft positions scored/s"
+    unit = "positions/s"
+    summary = "row_stats_kernel_b256_v128256_k5_bf16.md"
+    kernel = "row_stats_kernel<bf16, bf16 logits>"
+    sources = ("common.cuh", "row_stats.cuh")
+
+    def describe(self):
+        return {"workload": "acceptance statistics (sum min(p,q), KL(q||p), TV) per drafted position, B=256 "
+                            "V=128256 K=5 bf16 T=0.7, the headline sampling inputs", "B": B, "V": V, "K": K,
+                "temperature": T, "input_bytes": 2 * B * K * V * 2,
+                "l2": "inputs (657 MB read) larger than L2; no flush"}
+
+    def batch(self, seqs):
+        from speculative_decoding_verification_52_gb300 import inputs as gen
+        return gen.config_headline(seqs=seqs)
+
+    def units(self, batch):
+        return batch.B * batch.K
+
+    def algorithmic_bytes(self, batch):
+        # every target row t < K and every draft row, read once
+        return 2 * batch.B * batch.K * batch.V * 2
+
+    def oracle_call(self, batch, sl):
+        import oracle
+        oracle.row_stats(batch.target[sl], batch.dtype, batch.draft[sl], batch.dtype, False, batch.T)
+
+    def device_setup(self, batch, dev):
+        import torch
+
+        import speculative_decoding_verification_52_gb300 as sv
+        hs = [_bf16_host(batch.target), _bf16_host(batch.draft)]
+        ds = [h.to(dev) for h in hs]
+        outs = [torch.empty((batch.B, batch.K), dtype=torch.float32, device=dev) for _ in range(3)]
+        stream = torch.cuda.current_stream()
+
+        def step():
+            sv.spec_row_stats(ds[0], ds[1], batch.T, alpha=outs[0], kl=outs[1], tv=outs[2], stream=stream)
+        return hs, ds, step, outs
+
+
 WORKLOADS = {w.name: w for w in (SampleWorkload(), GreedyWorkload(), TreeWorkload(), TreeMaskWorkload(),
-                                 KvCommitWorkload())}
+                                 KvCommitWorkload(), StatsWorkload())}
 
 
 def oracle_rate(wl: Workload, batch, budget_s: float, min_seqs: int):
@@ -633,7 +686,7 @@ def run_ours(args, wl: Workload, ws, rank, local):
     cfg["metric_frac_of_8TBps"] = alg / (ms * 1e-3) / 8e12
     roof = {"bound": "hbm", "kernel": wl.kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm, "peak_source": f"{src} hbm_gbs (burst copy)",
-            "traffic": profiled_traffic(wl.summary), "algorithmic_bytes": alg, "avg_launch_ms": kern_avg_ms}
+            "traffic": profiled_traffic(wl.summary, wl.sources), "algorithmic_bytes": alg, "avg_launch_ms": kern_avg_ms}
     if wl.launches_per_step > 1:
         roof["finish_avg_ms"] = fin_avg_ms
     line = {

@@ -223,6 +223,30 @@ spec_status_t spec_kv_commit(void *cache, const int32_t *lengths, const void *sc
                              const int32_t *count, int B, int Lmax, int N, int W, size_t entry_bytes,
                              int32_t *new_lengths, void *stream);
 
+/* Acceptance statistics of a draft against its target, per drafted position
+ * ("Speculative decoding: draft, verify, repeat", step 4: acceptance rate
+ * against the divergence between the draft and the verifier; "Speculative
+ * Decoding: from idea to SOTA", section 3: x_t is accepted with probability
+ * min(1, p/q), so position t is accepted with probability sum_v min(p_t, q_t)).
+ *
+ *   target_logits [B, K+1, V], draft [B, K, V], draft_kind, temperature: as in
+ *       spec_verify_sample (the same buffers may be passed); row K of the
+ *       target is not read.  temperature must be > 0.
+ *   alpha, kl, tv [B, K] float32 (device, written):
+ *       alpha[b,t] = sum_v min(p_t(v), q_t(v)),
+ *       kl[b,t]    = KL(q_t || p_t) = sum_{v: q>0} q log(q / p) (natural log),
+ *       tv[b,t]    = 1/2 sum_v |p_t(v) - q_t(v)|.
+ *   An invalid row pair (a logit row with NaN or +inf or no finite entry; draft
+ *   probabilities with NaN or a negative entry) gives NaN in all three; -2 in all
+ *   three means an internal wait hit its time limit.
+ *
+ * Each row pair is read from HBM once (one thread-block cluster holds it in
+ * shared memory).  Limits: V * (target + draft element bytes) <= 1.6 MB, i.e.
+ * V <= 409600 for bf16 pairs (SPEC_ERR_UNSUPPORTED beyond); 1e-4 <= T. */
+spec_status_t spec_row_stats(const void *target_logits, spec_dtype_t target_dtype, const void *draft,
+                             spec_dtype_t draft_dtype, spec_draft_kind_t draft_kind, float temperature, int B,
+                             int K, int V, float *alpha, float *kl, float *tv, void *stream);
+
 /* Timing hooks for benchmarks: while enabled, each verify call records CUDA
  * events on the call's stream around its kernels (at most max_calls calls are
  * recorded).  spec_profile_end synchronises on the recorded events and returns

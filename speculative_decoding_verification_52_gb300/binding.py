@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
             L.spec_tree_mask.restype = I
             L.spec_kv_commit.argtypes = [P, P, P, P, P, I, I, I, I, Z, P, P]
             L.spec_kv_commit.restype = I
+            L.spec_row_stats.argtypes = [P, I, P, I, I, F, I, I, I, P, P, P, P]
+            L.spec_row_stats.restype = I
             L.spec_profile_begin.argtypes = [I]
             L.spec_profile_begin.restype = I
             L.spec_profile_end.argtypes = [P, P, P]
@@ -289,6 +291,29 @@ def spec_kv_commit(cache, lengths, scratch, count, *, path=None, new_lengths=Non
                               _ptr(new_lengths), _stream(stream))
     _check("spec_kv_commit", st)
     return new_lengths
+
+
+def spec_row_stats(target_logits, draft, temperature, *, draft_kind: str = "logits", alpha=None, kl=None,
+                   tv=None, stream=None):
+    """Per-position acceptance statistics.  target_logits [B,K+1,V] (bf16/f32),
+    draft [B,K,V] (logits: bf16/f32; probs: f32).  Returns (alpha, kl, tv), each
+    [B,K] f32: sum min(p,q), KL(q||p), TV(p,q)."""
+    _dev(target_logits, "target_logits")
+    _dev(draft, "draft")
+    B, W, V = target_logits.shape
+    K = W - 1
+    kind = SPEC_DRAFT_PROBS if draft_kind == "probs" else SPEC_DRAFT_LOGITS
+    outs = []
+    for o, n in ((alpha, "alpha"), (kl, "kl"), (tv, "tv")):
+        if o is None:
+            o = torch.empty((B, K), dtype=torch.float32, device=target_logits.device)
+        _dev(o, n)
+        outs.append(o)
+    st = lib().spec_row_stats(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), _dtype_code(draft), kind,
+                              float(temperature), B, K, V, _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]),
+                              _stream(stream))
+    _check("spec_row_stats", st)
+    return tuple(outs)
 
 
 def spec_profile_begin(max_calls: int):

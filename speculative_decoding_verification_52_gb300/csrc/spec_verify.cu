@@ -27,6 +27,7 @@
 #include "tree.cuh"
 #include "tree_mask.cuh"
 #include "kv_commit.cuh"
+#include "row_stats.cuh"
 
 namespace {
 
@@ -620,6 +621,46 @@ spec_status_t sample_entry(const void* target, spec_dtype_t tdt, const void* dra
                          nacc, ws, debug_b, debug_t, drow, dmass, st);
 }
 
+// ---------------------------------------------------------------------------
+// acceptance statistics (one cluster per position pair)
+// ---------------------------------------------------------------------------
+// Slice length and cluster size: the smallest power-of-two cluster (up to 8)
+// whose per-CTA slice pair fits RS_TARGET_SMEM; beyond that the cluster stays at
+// 8 and the slice grows up to RS_MAX_SMEM.  L is a multiple of 16 elements so
+// every slice starts 16-byte aligned; CS = ceil(V / L) leaves no empty CTA.
+bool row_stats_shape(int V, int bytes_per_pair, int& L, int& CS) {
+  auto slice = [&](int cs) { return (ceil_div(V, cs) + 15) / 16 * 16; };
+  int cs = 1;
+  while (cs < RS_MAX_CLUSTER && static_cast<long long>(slice(cs)) * bytes_per_pair > RS_TARGET_SMEM) cs *= 2;
+  L = slice(cs);
+  CS = ceil_div(V, L);
+  return static_cast<long long>(L) * bytes_per_pair <= RS_MAX_SMEM;
+}
+
+template <class TP, class TQ, bool PROBS>
+spec_status_t launch_row_stats(int dev, const RowStatsArgs& a, cudaStream_t st) {
+  auto kern = row_stats_kernel<TP, TQ, PROBS>;
+  if (!once_per_device(dev, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RS_MAX_SMEM) == cudaSuccess;
+      }))
+    return fail(SPEC_ERR_CUDA, "row stats kernel setup failed: %s", cudaGetErrorString(cudaGetLastError()));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.B) * a.K * a.CS));
+  cfg.blockDim = dim3(RS_THREADS);
+  cfg.dynamicSmemBytes = static_cast<size_t>(a.L) * (TP::esz + TQ::esz);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(a.CS);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return cuda_fail(e, "row stats launch");
+  return SPEC_OK;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -896,6 +937,64 @@ spec_status_t spec_kv_commit(void* cache, const int32_t* lengths, const void* sc
     kv_commit_kernel<<<grid, KV_THREADS, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kv commit launch");
+    prof_mark(1, st);
+    prof_mark(2, st);
+    return SPEC_OK;
+  } catch (...) {
+    return fail(SPEC_ERR_CUDA, "unexpected host exception");
+  }
+}
+
+spec_status_t spec_row_stats(const void* target_logits, spec_dtype_t target_dtype, const void* draft,
+                             spec_dtype_t draft_dtype, spec_draft_kind_t draft_kind, float temperature, int B, int K,
+                             int V, float* alpha, float* kl, float* tv, void* stream) {
+  try {
+    if (B < 0 || K < 0 || K > SPEC_MAX_K || V < 1)
+      return fail(SPEC_ERR_INVALID_ARG, "bad sizes B=%d K=%d V=%d", B, K, V);
+    if (!dtype_ok(target_dtype) || !dtype_ok(draft_dtype)) return fail(SPEC_ERR_INVALID_ARG, "bad dtype");
+    if (draft_kind != SPEC_DRAFT_LOGITS && draft_kind != SPEC_DRAFT_PROBS)
+      return fail(SPEC_ERR_INVALID_ARG, "bad draft kind");
+    const bool probs = draft_kind == SPEC_DRAFT_PROBS;
+    if (probs && draft_dtype != SPEC_F32) return fail(SPEC_ERR_INVALID_ARG, "draft probabilities must be float32");
+    if (!(temperature > 0.f) || !std::isfinite(temperature))
+      return fail(SPEC_ERR_INVALID_ARG, "temperature must be > 0 and finite");
+    if (temperature < 1e-4f) return fail(SPEC_ERR_UNSUPPORTED, "temperature %g below 1e-4", temperature);
+    if (B == 0 || K == 0) return SPEC_OK;
+    if (!target_logits || !draft || !alpha || !kl || !tv)
+      return fail(SPEC_ERR_INVALID_ARG, "NULL target/draft/alpha/kl/tv");
+    const int ep = esz_of(target_dtype), eq = esz_of(draft_dtype);
+    RowStatsArgs a{};
+    a.target = static_cast<const unsigned char*>(target_logits);
+    a.draft = static_cast<const unsigned char*>(draft);
+    a.B = B;
+    a.K = K;
+    a.V = V;
+    if (!row_stats_shape(V, ep + eq, a.L, a.CS))
+      return fail(SPEC_ERR_UNSUPPORTED, "V=%d: a slice pair of %d bytes per CTA exceeds %d", V, a.L * (ep + eq),
+                  RS_MAX_SMEM);
+    if (static_cast<long long>(B) * K * a.CS > 0x7fffffffLL) return fail(SPEC_ERR_UNSUPPORTED, "grid too large");
+    int dev;
+    DevInfo di;
+    spec_status_t s = device_info(di, dev);
+    if (s != SPEC_OK) return s;
+    a.vec = aligned16(target_logits) && aligned16(draft) && (static_cast<long long>(V) * ep) % 16 == 0 &&
+            (static_cast<long long>(V) * eq) % 16 == 0;
+    a.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+    a.alpha = alpha;
+    a.kl = kl;
+    a.tv = tv;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    prof_mark(0, st);
+    if (probs)
+      s = target_dtype == SPEC_BF16 ? launch_row_stats<BF16T, F32T, true>(dev, a, st)
+                                    : launch_row_stats<F32T, F32T, true>(dev, a, st);
+    else if (target_dtype == SPEC_BF16)
+      s = draft_dtype == SPEC_BF16 ? launch_row_stats<BF16T, BF16T, false>(dev, a, st)
+                                   : launch_row_stats<BF16T, F32T, false>(dev, a, st);
+    else
+      s = draft_dtype == SPEC_BF16 ? launch_row_stats<F32T, BF16T, false>(dev, a, st)
+                                   : launch_row_stats<F32T, F32T, false>(dev, a, st);
+    if (s != SPEC_OK) return s;
     prof_mark(1, st);
     prof_mark(2, st);
     return SPEC_OK;

@@ -125,3 +125,30 @@ def test_tree_mask_and_kv_commit_reject_bad_arguments(L):
     assert kv(P(16), P(32), P(48), None, P(64), 2, 8, 4, 0, 0, P(80), None) == B.SPEC_ERR_INVALID_ARG
     assert kv(P(16), None, P(48), None, P(64), 2, 8, 4, 0, 64, P(80), None) == B.SPEC_ERR_INVALID_ARG
     assert kv(None, None, None, None, None, 0, 8, 4, 0, 64, None, None) == B.SPEC_OK
+
+
+def test_row_stats_rejects_bad_arguments(L):
+    P, F = ctypes.c_void_p, ctypes.c_float
+    rs = L.spec_row_stats
+    ok = dict(t=P(16), td=B.SPEC_BF16, d=P(32), dd=B.SPEC_BF16, kind=B.SPEC_DRAFT_LOGITS, T=F(0.7), Bn=2, K=3,
+              V=64, a=P(48), k=P(64), v=P(80))
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return rs(a["t"], a["td"], a["d"], a["dd"], a["kind"], a["T"], a["Bn"], a["K"], a["V"], a["a"], a["k"],
+                  a["v"], None)
+
+    assert call(T=F(0.0)) == B.SPEC_ERR_INVALID_ARG
+    assert call(T=F(float("nan"))) == B.SPEC_ERR_INVALID_ARG
+    assert call(T=F(1e-5)) == B.SPEC_ERR_UNSUPPORTED
+    assert call(K=-1) == B.SPEC_ERR_INVALID_ARG
+    assert call(K=B.SPEC_MAX_K + 1) == B.SPEC_ERR_INVALID_ARG
+    assert call(V=0) == B.SPEC_ERR_INVALID_ARG
+    assert call(td=7) == B.SPEC_ERR_INVALID_ARG
+    assert call(kind=B.SPEC_DRAFT_PROBS) == B.SPEC_ERR_INVALID_ARG       # probabilities must be f32
+    assert call(kind=5) == B.SPEC_ERR_INVALID_ARG
+    assert call(a=None) == B.SPEC_ERR_INVALID_ARG
+    assert call(d=None) == B.SPEC_ERR_INVALID_ARG
+    assert call(V=1_000_000) == B.SPEC_ERR_UNSUPPORTED       # slice pair beyond the limit
+    assert call(Bn=0, t=None, d=None, a=None) == B.SPEC_OK
+    assert call(K=0, t=None, d=None, a=None) == B.SPEC_OK

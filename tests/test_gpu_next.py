@@ -86,3 +86,107 @@ def test_commit_after_tree_verification(orc):
     np.testing.assert_array_equal(newl.cpu().numpy(), ref_len)
     np.testing.assert_array_equal(c.cpu().numpy(), ref_cache)
     assert (ref_len - lengths == rn).all()
+
+
+# --- acceptance statistics --------------------------------------------------------
+# Tolerances (fp32 path against the double oracle): every summed term carries the
+# ex2 approximation's relative error (a few 1e-7) and the normalisers one more
+# such factor each, so alpha and TV (sums of terms <= 1 that total <= 1) are
+# within 2e-6; KL combines O(10)-sized log-domain terms whose fp32 rounding is
+# ~1e-6 each, so it is checked to 1e-5 absolute plus 1e-5 relative.
+ALPHA_TOL, KL_ABS, KL_REL = 2e-6, 1e-5, 1e-5
+
+
+def _softmax_probs(draft, dtype, T):
+    y = gen.as_f64(draft, dtype) / T
+    y -= y.max(-1, keepdims=True)
+    e = np.exp(y)
+    return (e / e.sum(-1, keepdims=True)).astype(np.float32)
+
+
+def _stats_pair(orc, target, tdt, draft, ddt, T, probs=False):
+    g = sv.spec_row_stats(gu.dev_tensor(target, tdt), gu.dev_tensor(draft, ddt), T,
+                          draft_kind="probs" if probs else "logits")
+    g = [x.cpu().numpy().astype(np.float64) for x in g]
+    r = orc.row_stats(target, tdt, draft, ddt, probs, T)
+    for name, gv, rv in zip(("alpha", "kl", "tv"), g, r):
+        np.testing.assert_array_equal(np.isnan(gv), np.isnan(rv), err_msg=f"{name}: invalid rows differ")
+        ok = ~np.isnan(rv)
+        if name == "kl":
+            np.testing.assert_allclose(gv[ok], rv[ok], rtol=KL_REL, atol=KL_ABS, err_msg=name)
+        else:
+            np.testing.assert_allclose(gv[ok], rv[ok], rtol=0, atol=ALPHA_TOL, err_msg=name)
+    return g, r
+
+
+@pytest.mark.parametrize("V,dtype", [(128256, "bf16"), (32000, "f32"), (1000, "bf16"), (999, "bf16"),
+                                     (37, "f32"), (77777, "bf16"), (8, "f32")])
+def test_row_stats_match_oracle(orc, V, dtype):
+    """Cluster sizes 8, 4 and 1; bulk-copied rows and (odd V) element loads."""
+    b = gen.gaussian_chain(6, V, 5, sigma=0.445, T=0.7, dtype=dtype, seed=52_310 + V)
+    _stats_pair(orc, b.target, dtype, b.draft, dtype, 0.7)
+
+
+def test_row_stats_zipf_and_mixed_dtypes(orc):
+    b = gen.config_zipf(seqs=range(6))
+    _stats_pair(orc, b.target, "f32", b.draft, "f32", 1.0)
+    h = gen.config_headline(seqs=range(3), V=4096)
+    d32 = gen.as_f64(h.draft, "bf16").astype(np.float32)
+    _stats_pair(orc, h.target, "bf16", d32, "f32", 0.7)
+    t32 = gen.as_f64(h.target, "bf16").astype(np.float32)
+    _stats_pair(orc, t32, "f32", h.draft, "bf16", 0.7)
+
+
+@pytest.mark.parametrize("tdt", ["bf16", "f32"])
+def test_row_stats_draft_probabilities(orc, tdt):
+    h = gen.config_headline(seqs=range(4), V=32000, K=4)
+    target = h.target if tdt == "bf16" else gen.as_f64(h.target, "bf16").astype(np.float32)
+    q = _softmax_probs(h.draft, "bf16", 0.7)
+    q[1, 2, :] = 0.0
+    q[1, 2, 17] = 1.0                      # one-hot draft: alpha = p(17), KL = -log p(17)
+    q[2, 0, ::3] = 0.0                     # zeros skipped by the KL sum
+    g, r = _stats_pair(orc, target, tdt, q, "f32", 0.7, probs=True)
+    assert g[0][1, 2] < 1e-3
+
+
+def test_row_stats_identical_and_controlled(orc):
+    """Bit-identical draft rows give alpha = 1, KL = 0, TV = 0 (V = 151936)."""
+    b = gen.config_controlled(4, 4, seqs=range(4))
+    g, _ = _stats_pair(orc, b.target, "bf16", b.draft, "bf16", 1.0)
+    cp = b.meta["copied"]
+    assert cp.any() and (~cp).any()
+    np.testing.assert_allclose(g[0][cp], 1.0, atol=ALPHA_TOL)
+    assert (g[1][cp] == 0.0).all()
+
+
+def test_row_stats_invalid_rows(orc):
+    b = gen.gaussian_chain(4, 4096, 3, sigma=0.5, T=1.0, dtype="f32", seed=52_390)
+    t, d = b.target.copy(), b.draft.copy()
+    t[0, 1, 100] = np.nan
+    d[1, 0, 5] = np.inf
+    t[2, 2, :] = -np.inf
+    t[3, 0, :] = -np.inf
+    t[3, 0, 9] = 0.5                       # one finite entry: valid (p is one-hot)
+    g, r = _stats_pair(orc, t, "f32", d, "f32", 1.0)
+    assert np.isnan(g[0][0, 1]) and np.isnan(g[0][1, 0]) and np.isnan(g[0][2, 2])
+    assert np.isfinite(g[0]).sum() == 12 - 3
+    q = _softmax_probs(b.draft, "f32", 1.0)
+    q[0, 0, 3] = -1e-3
+    q[1, 1, 8] = np.nan
+    g, _ = _stats_pair(orc, b.target, "f32", q, "f32", 1.0, probs=True)
+    assert np.isnan(g[0][0, 0]) and np.isnan(g[0][1, 1]) and np.isfinite(g[0]).sum() == 10
+
+
+def test_row_stats_full_headline_batch(orc):
+    """B=256, V=128256, K=5 bf16, T=0.7 in the benchmark's launch configuration;
+    every position against the oracle, and the mean alpha of the workload."""
+    b = gen.config_headline()
+    g, r = _stats_pair(orc, b.target, "bf16", b.draft, "bf16", 0.7)
+    assert abs(r[0].mean() - 0.75) < 0.01
+
+
+def test_row_stats_empty():
+    t = torch.zeros((3, 1, 64), dtype=torch.bfloat16, device=gu.DEV)
+    d = torch.zeros((3, 0, 64), dtype=torch.bfloat16, device=gu.DEV)
+    a, k, tv = sv.spec_row_stats(t, d, 1.0)
+    assert a.shape == (3, 0)
