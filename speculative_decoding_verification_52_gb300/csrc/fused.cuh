@@ -182,13 +182,56 @@ __device__ __forceinline__ float2 two_sum(float a, float b) {
   return make_float2(s, e);
 }
 
-// 2^x for a double x <= 0 with ~1e-7 relative accuracy, without a double
-// exp2: the accurate fp32 exp2f of the leading part, corrected to first order
-// for the remainder
-__device__ __forceinline__ double exp2_d(double x) {
-  const float xf = static_cast<float>(x);
-  const double r = x - static_cast<double>(xf);
-  return static_cast<double>(exp2f(xf)) * (1.0 + r * 0.6931471805599453);
+// Float-float numbers (hi + lo, |lo| <= ulp(hi)/2): ~48 significant bits on
+// the fp32 pipes.  The finishing warps sum, scan and compare in this form;
+// GB300's fp64 rate is a small fraction of its fp32 rate, and these steps sit
+// on the latency path at the end of every launch.
+struct FF {
+  float hi, lo;
+};
+__device__ __forceinline__ FF ff_norm(float hi, float lo) {   // |hi| >= |lo|
+  const float s = __fadd_rn(hi, lo);
+  return FF{s, __fsub_rn(lo, __fsub_rn(s, hi))};
+}
+__device__ __forceinline__ FF ff_add_f(FF a, float b) {
+  const float2 t = two_sum(a.hi, b);
+  return ff_norm(t.x, __fadd_rn(t.y, a.lo));
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const float2 t = two_sum(a.hi, b.hi);
+  return ff_norm(t.x, __fadd_rn(t.y, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ FF ff_sub(FF a, FF b) { return ff_add(a, FF{-b.hi, -b.lo}); }
+__device__ __forceinline__ FF ff_mul_f(FF a, float b) {
+  const float p = __fmul_rn(a.hi, b);
+  const float e = __fmaf_rn(a.hi, b, -p);   // the product's rounding error, exactly
+  return ff_norm(p, __fmaf_rn(a.lo, b, e));
+}
+// a > b
+__device__ __forceinline__ bool ff_gt(FF a, FF b) {
+  return __fadd_rn(__fsub_rn(a.hi, b.hi), __fsub_rn(a.lo, b.lo)) > 0.f;
+}
+__device__ __forceinline__ float ff_to_f(FF a) { return __fadd_rn(a.hi, a.lo); }
+__device__ __forceinline__ FF ff_shfl_xor(FF a, int o) {
+  return FF{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ FF ff_shfl_up(FF a, int o) {
+  return FF{__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ FF ff_shfl(FF a, int l) {
+  return FF{__shfl_sync(0xffffffffu, a.hi, l), __shfl_sync(0xffffffffu, a.lo, l)};
+}
+
+// 2^(z*c - A) for an fp32 logit z, c = log2(e)/T and A = fl(M*c): the exponent
+// is formed exactly as a float-float (the product's error by fma, the
+// difference by two-sum), then the accurate fp32 exp2f of its leading part is
+// corrected to first order for the remainder (~1e-7 relative accuracy)
+__device__ __forceinline__ float exp2_arg_ff(float z, float c, float A) {
+  const float p = __fmul_rn(z, c);
+  const float pe = __fmaf_rn(z, c, -p);
+  const float2 x = two_sum(p, -A);
+  const float r = __fadd_rn(x.y, pe);
+  return __fmul_rn(exp2f(x.x), __fmaf_rn(r, 0.69314718f, 1.f));
 }
 
 // ---------------------------------------------------------------------------
@@ -310,20 +353,26 @@ __device__ __forceinline__ T row_get(const T (&v)[2], int r) {   // row r lives 
   const T v1 = __shfl_sync(0xffffffffu, v[1], r & 31);
   return r < 32 ? v0 : v1;
 }
+__device__ __forceinline__ FF row_get_ff(const FF (&v)[2], int r) {
+  const FF v0 = ff_shfl(v[0], r & 31);
+  const FF v1 = ff_shfl(v[1], r & 31);
+  return r < 32 ? v0 : v1;
+}
 
 // Inputs of position `lane` of sequence b that do not depend on the sweep:
 // the drafted token, its target and draft logits (or draft probability) and
-// the accept uniform.  The finisher loads them while it waits for the
+// the accept and draw uniforms.  The finisher loads them while it waits for the
 // sequence's sweep to complete.
 struct ScanInputs {
   int x;
-  float zp, zq, u0;
+  float zp, zq, u0, u1;   // u1: the replacement-draw uniform of position `lane` (lanes 0..K)
 };
 
 template <class TP, class TQ, bool PROBS>
 __device__ __forceinline__ ScanInputs scan_inputs(const FusedArgs& a, int b, int lane) {
   const int K = a.K, W = K + 1, V = a.V;
-  ScanInputs in{-1, 0.f, 0.f, 0.f};
+  ScanInputs in{-1, 0.f, 0.f, 0.f, 0.f};
+  if (lane < W) in.u1 = a.uni[(static_cast<long long>(b) * W + lane) * 2 + 1];
   if (lane < K) {
     in.x = a.tokens[static_cast<long long>(b) * K + lane];
     in.u0 = a.uni[(static_cast<long long>(b) * W + lane) * 2];
@@ -365,7 +414,7 @@ __device__ __forceinline__ float4 merge_unit(float2 p, int lane, float c) {
 // Merge the S unit partials of row r of sequence b (one lane): online
 // float-float accumulation relative to the running maximum.  Row r lands in
 // slot r >> 5 of this lane (lane r & 31).
-__device__ __forceinline__ void merge_row(const FusedArgs& a, int b, int r, float (&Ar)[2], double (&Sr)[2],
+__device__ __forceinline__ void merge_row(const FusedArgs& a, int b, int r, float (&Ar)[2], FF (&Sr)[2],
                                           int (&st)[2]) {
   const float4* up = a.part + (static_cast<long long>(b) * a.RB + r) * a.S;
   float M = kNegInf, hi = 0.f, lo = 0.f;
@@ -394,10 +443,10 @@ __device__ __forceinline__ void merge_row(const FusedArgs& a, int b, int r, floa
     hi = t.x;
     lo += t.y + fmaf(u.y, f, -h) + u.z * f;
   }
-  const double acc = static_cast<double>(hi) + static_cast<double>(lo);
+  const FF acc = ff_norm(hi, lo);
   Ar[r >> 5] = (bad || M == kNegInf) ? 0.f : __fmul_rn(M, c);
   Sr[r >> 5] = acc;
-  st[r >> 5] = bad ? 2 : (M == kNegInf ? 1 : ((isfinite(acc) && acc > 0.0) ? 0 : 1));
+  st[r >> 5] = bad ? 2 : (M == kNegInf ? 1 : ((isfinite(acc.hi) && acc.hi > 0.f) ? 0 : 1));
 }
 
 template <class TP, class TQ, bool PROBS>
@@ -406,7 +455,7 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
   const int x = in.x;
   const float u0 = in.u0;
   float Ar[2] = {0.f, 0.f};
-  double Sr[2] = {0.0, 0.0};
+  FF Sr[2] = {FF{0.f, 0.f}, FF{0.f, 0.f}};
   int st[2] = {1, 1};
   // lane r merges row r (and row r + 32 when there are more than 32 rows)
   if (lane < a.RB) merge_row(a, b, lane, Ar, Sr, st);
@@ -417,7 +466,7 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
   const int rp = t < W ? t : 0;
   const int rq = (t < K && !PROBS) ? W + t : 0;
   const float At = row_get(Ar, rp), Aq = row_get(Ar, rq);
-  const double St = row_get(Sr, rp), Sq = row_get(Sr, rq);
+  const FF St = row_get_ff(Sr, rp), Sq = row_get_ff(Sr, rq);
   const int stt = row_get(st, rp), stq = row_get(st, rq);
   bool tok_bad = false, acc_t = true;
   int row_bad = 0;   // rows read at position t: 0 ok, 1 invalid, 2 poisoned
@@ -427,20 +476,20 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
     if (!PROBS && row_bad == 0) row_bad = stq;
     if (!tok_bad && row_bad == 0) {
       // accept iff q(x) == 0 or u < p(x)/q(x), with p(x) = ep / St and q(x) = eq / Sq:
-      // u * St * eq < ep * Sq, no division
-      const double cd = static_cast<double>(a.c);
+      // u * St * eq < ep * Sq, no division (float-float products)
       const float zpf = in.zp, zqf = in.zq;
-      const double ep = exp2_d(static_cast<double>(zpf) * cd - static_cast<double>(At));
-      double eq, Sqq;
+      const float ep = exp2_arg_ff(zpf, a.c, At);
+      float eq;
+      FF Sqq;
       if (PROBS) {
         if (zqf != zqf || zqf < 0.f) row_bad = 1;
-        eq = static_cast<double>(zqf);
-        Sqq = 1.0;
+        eq = zqf;
+        Sqq = FF{1.f, 0.f};
       } else {
-        eq = exp2_d(static_cast<double>(zqf) * cd - static_cast<double>(Aq));
+        eq = exp2_arg_ff(zqf, a.c, Aq);
         Sqq = Sq;
       }
-      acc_t = (eq == 0.0) || (static_cast<double>(u0) * St * eq < ep * Sqq);
+      acc_t = (eq == 0.f) || ff_gt(ff_mul_f(Sqq, ep), ff_mul_f(ff_mul_f(St, u0), eq));
     }
   }
   const unsigned badtok = __ballot_sync(0xffffffffu, t < K && tok_bad);
@@ -461,10 +510,11 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
   const int sq_state = row_get(st, has_q ? W + tstar : 0);
   if (status == 0 && has_q && sq_state != 0) status = sq_state == 2 ? -2 : -1;
   const float Ap = row_get(Ar, tstar);
-  const double Sp = row_get(Sr, tstar);
+  const FF Sp = row_get_ff(Sr, tstar);
   const float Aq2 = row_get(Ar, has_q ? W + tstar : 0);
-  const double Sq2 = row_get(Sr, has_q ? W + tstar : 0);
+  const FF Sq2 = row_get_ff(Sr, has_q ? W + tstar : 0);
 
+  const float u1 = __shfl_sync(0xffffffffu, in.u1, tstar);
   // accepted prefix (slot tstar is written by the pick), -1 padding
   int32_t* out = a.out_tokens + static_cast<long long>(b) * W;
   const int x_all = x;
@@ -479,9 +529,9 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
     inf.tstar = tstar;
     inf.AP = Ap;
     inf.AQ = has_q ? Aq2 : 0.f;
-    inf.iSp = __frcp_rn(static_cast<float>(Sp));   // scales of the residual weights: fp32 suffices
-    inf.iSq = has_q ? __frcp_rn(static_cast<float>(Sq2)) : 1.f;
-    inf.u1 = a.uni[(static_cast<long long>(b) * W + tstar) * 2 + 1];
+    inf.iSp = __frcp_rn(ff_to_f(Sp));   // scales of the residual weights: fp32 suffices
+    inf.iSq = has_q ? __frcp_rn(ff_to_f(Sq2)) : 1.f;
+    inf.u1 = u1;
     inf.pad = 0.f;
     a.info[b] = inf;
   }
@@ -512,10 +562,10 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
   float bv[kRegBlocks];
 #pragma unroll
   for (int k = 0; k < kRegBlocks; ++k) bv[k] = (bl0 + k < bl1) ? __ldcg(brow + bl0 + k) : 0.f;
-  double lsum = 0.0;
+  FF lsum{0.f, 0.f};
 #pragma unroll
-  for (int k = 0; k < kRegBlocks; ++k) lsum += static_cast<double>(bv[k]);
-  for (int k = bl0 + kRegBlocks; k < bl1; ++k) lsum += static_cast<double>(__ldcg(brow + k));
+  for (int k = 0; k < kRegBlocks; ++k) lsum = ff_add_f(lsum, bv[k]);
+  for (int k = bl0 + kRegBlocks; k < bl1; ++k) lsum = ff_add_f(lsum, __ldcg(brow + k));
   if (inf.status != 0) return;   // outputs already written by the scan
   const unsigned char* prow = a.target + (static_cast<long long>(b) * W + inf.tstar) * V * TP::esz;
   const unsigned char* qrow =
@@ -532,21 +582,21 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
       w[i] = resid_w(zp[i], has_q ? zq[i] : 0.f, c, -inf.AP, -inf.AQ, inf.iSp, inf.iSq, has_q, PROBS);
   };
 
-  double R = 0.0;
+  FF R{0.f, 0.f};
   for (int pass = 0; pass < 2; ++pass) {
     if (pass > 0) {
-      lsum = 0.0;
+      lsum = FF{0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < kRegBlocks; ++k) {
         bv[k] = (bl0 + k < bl1) ? __ldcg(brow + bl0 + k) : 0.f;
-        lsum += static_cast<double>(bv[k]);
+        lsum = ff_add_f(lsum, bv[k]);
       }
-      for (int k = bl0 + kRegBlocks; k < bl1; ++k) lsum += static_cast<double>(__ldcg(brow + k));
+      for (int k = bl0 + kRegBlocks; k < bl1; ++k) lsum = ff_add_f(lsum, __ldcg(brow + k));
     }
     R = lsum;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) R += __shfl_xor_sync(0xffffffffu, R, o);
-    if (R > 0.0 || !has_q) break;
+    for (int o = 16; o > 0; o >>= 1) R = ff_add(R, ff_shfl_xor(R, o));
+    if (R.hi > 0.f || !has_q) break;
     // residual mass zero: draw from p_t instead (rebuild the block sums; rare)
     has_q = false;
     for (int blk = 0; blk < NB; ++blk) {
@@ -565,36 +615,39 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
     __syncwarp();
     __threadfence_block();
   }
-  const double target = static_cast<double>(inf.u1) * R;
+  const FF target = ff_mul_f(R, inf.u1);
   // exclusive prefix of the lanes' block ranges, then the block holding the target
-  double incl = lsum;
+  FF incl = lsum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+    const FF y = ff_shfl_up(incl, o);
+    if (lane >= o) incl = ff_add(incl, y);
   }
   int jb = -1, jlast = -1;
-  double jbase = 0.0, lastbase = 0.0;
+  FF jbase{0.f, 0.f}, lastbase{0.f, 0.f};
   {
-    double run = incl - lsum;
+    FF run = ff_shfl_up(incl, 1);
+    if (lane == 0) run = FF{0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < kRegBlocks; ++k) {
-      const double v = static_cast<double>(bv[k]);
-      if (v > 0.0) {
+      const float v = bv[k];
+      const FF nxt = ff_add_f(run, v);
+      if (v > 0.f) {
         jlast = bl0 + k;
         lastbase = run;
-        if (jb < 0 && run + v > target) { jb = bl0 + k; jbase = run; }
+        if (jb < 0 && ff_gt(nxt, target)) { jb = bl0 + k; jbase = run; }
       }
-      run += v;
+      run = nxt;
     }
     for (int k = bl0 + kRegBlocks; k < bl1; ++k) {
-      const double v = static_cast<double>(__ldcg(brow + k));
-      if (v > 0.0) {
+      const float v = __ldcg(brow + k);
+      const FF nxt = ff_add_f(run, v);
+      if (v > 0.f) {
         jlast = k;
         lastbase = run;
-        if (jb < 0 && run + v > target) { jb = k; jbase = run; }
+        if (jb < 0 && ff_gt(nxt, target)) { jb = k; jbase = run; }
       }
-      run += v;
+      run = nxt;
     }
   }
   const unsigned hit = __ballot_sync(0xffffffffu, jb >= 0);
@@ -607,7 +660,7 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
   int pick = -1;
   if (src_lane >= 0) {
     const int blk = __shfl_sync(0xffffffffu, exact ? jb : jlast, src_lane);
-    const double bb = __shfl_sync(0xffffffffu, exact ? jbase : lastbase, src_lane);
+    const FF bb = ff_shfl(exact ? jbase : lastbase, src_lane);
     // re-read the block: lane l holds elements blk*256 + 8l .. +8
     const int e = blk * FU_BLK + 8 * lane;
     float w[8];
@@ -620,18 +673,20 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) w[i] = 0.f;
     }
-    double x2 = static_cast<double>(s);
+    FF x2{s, 0.f};
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, x2, o);
-      if (lane >= o) x2 += y;
+      const FF y = ff_shfl_up(x2, o);
+      if (lane >= o) x2 = ff_add(x2, y);
     }
-    const double lb = bb + (x2 - static_cast<double>(s));
+    FF ex = ff_shfl_up(x2, 1);
+    if (lane == 0) ex = FF{0.f, 0.f};
+    const FF lb = ff_add(bb, ex);
     int cand = 0x7fffffff, lastpos = -1;
-    if (s > 0.f && lb <= target && lb + static_cast<double>(s) > target) {
+    if (s > 0.f && !ff_gt(lb, target) && ff_gt(ff_add_f(lb, s), target)) {
       // the lane holding the target: search its 8 weights against the
       // remaining mass (in fp32; the lane's own sum is exact enough here)
-      const float rem = static_cast<float>(target - lb);
+      const float rem = ff_to_f(ff_sub(target, lb));
       float run = 0.f;
       int lastw = -1;
 #pragma unroll
@@ -653,14 +708,16 @@ __device__ void finish_pick(const FusedArgs& a, int b, int lane) {
     pick = cand != 0x7fffffff ? cand : lastpos;
   }
   if (lane == 0) a.out_tokens[static_cast<long long>(b) * W + inf.tstar] = pick;
-  if (b == a.debug_b && R > 0.0) {
+  if (b == a.debug_b && R.hi > 0.f) {
     for (int e = 8 * lane; e < V; e += 256) {
       float w[8];
       weights8(e, w);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a.debug_row[e + i] = static_cast<float>(static_cast<double>(w[i]) / R);
+      for (int i = 0; i < 8; ++i)
+        a.debug_row[e + i] =
+            static_cast<float>(static_cast<double>(w[i]) / (static_cast<double>(R.hi) + static_cast<double>(R.lo)));
     }
-    if (lane == 0) *a.debug_mass = static_cast<float>(R);
+    if (lane == 0) *a.debug_mass = ff_to_f(R);
   }
 }
 
