@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
             L.orc_row_stats.argtypes = [P, I, P, I, I, D, I, I, I, P, P, P]
             L.orc_row_stats.restype = I
             L.orc_verify_tree_greedy.restype = I
+            L.orc_tree_draft.argtypes = [P, I, P, I, I, I, D, P, P]
+            L.orc_tree_draft.restype = I
             _lib = L
     return _lib
 
@@ -262,3 +264,17 @@ def row_stats(target, target_dtype, draft, draft_dtype, draft_is_probs, T: float
     if rc:
         raise MemoryError("oracle allocation failed")
     return tuple(out)
+
+
+def tree_draft(draft, dtype, parents, T: float):
+    """Top-k tree drafting: (node_tokens [B, N] int32, node_logq [B, N] f64, rc);
+    rc = 1 for a malformed topology."""
+    d = _raw(draft, dtype)
+    B, N, V = d.shape
+    par = np.ascontiguousarray(parents, dtype=np.int32)
+    tok = np.empty((B, N), np.int32)
+    lq = np.empty((B, N), np.float64)
+    rc = lib().orc_tree_draft(_ptr(d), _dt(dtype), _ptr(par), B, N, V, float(T), _ptr(tok), _ptr(lq))
+    if rc == 2:
+        raise MemoryError("oracle allocation failed")
+    return tok, lq, rc

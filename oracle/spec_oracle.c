@@ -497,3 +497,64 @@ int orc_row_stats(const void *target, int target_dtype, const void *draft, int d
   free(z); free(p); free(q);
   return 0;
 }
+
+/* Top-k tree drafting ([SDE] "Make it": an EAGLE-style drafter builds a tree of
+ * depth K whose branches are the top-k tokens at each node; exercise 4: the
+ * top-3 branches at each depth instead of a chain; [SDE] "EAGLE": K = 4-8
+ * candidates per depth).
+ *
+ * draft [B, N, V]: one draft logit row per tree node; row p is the draft's
+ * distribution for the token after node p.  parents [N] (parents[0] = -1,
+ * 0 <= parents[i] < i).  The children of node p, taken in increasing index
+ * order, receive the tokens of row p in decreasing logit order (equal logits:
+ * the smaller vocabulary index first): child r gets the r-th largest.
+ * node_logq[b, i] = log q(token) with q = softmax(row p / T), the draft
+ * probability of the child's token.  Node 0 gets token -1 and log q 0.  A
+ * child whose rank is >= V gets -1 / NaN; so do the children of an invalid row
+ * (NaN, +inf, or no finite entry).  A malformed topology gives -1 / NaN for
+ * every node of every sequence and returns 1. */
+int orc_tree_draft(const void *draft, int dtype, const int32_t *parents, int B, int N, int V, double T,
+                   int32_t *node_tokens, double *node_logq) {
+  int ok = (N >= 1 && parents[0] == -1);
+  for (int i = 1; ok && i < N; ++i)
+    if (parents[i] < 0 || parents[i] >= i) ok = 0;
+  if (!ok) {
+    for (size_t k = 0; k < (size_t)B * N; ++k) { node_tokens[k] = -1; node_logq[k] = NAN; }
+    return 1;
+  }
+  double *z = (double *)malloc(sizeof(double) * (size_t)V);
+  double *p = (double *)malloc(sizeof(double) * (size_t)V);
+  char *taken = (char *)malloc((size_t)V);
+  if (!z || !p || !taken) { free(z); free(p); free(taken); return 2; }
+  for (int b = 0; b < B; ++b) {
+    int32_t *tok = node_tokens + (size_t)b * N;
+    double *lq = node_logq + (size_t)b * N;
+    tok[0] = -1;
+    lq[0] = 0.0;
+    for (int par = 0; par < N; ++par) {
+      int nchild = 0;
+      for (int i = par + 1; i < N; ++i)
+        if (parents[i] == par) ++nchild;
+      if (nchild == 0) continue;
+      orc_widen_row(draft, dtype, ((size_t)b * N + (size_t)par) * (size_t)V, V, z);
+      const int bad = orc_softmax(z, V, T, p);
+      for (int v = 0; v < V; ++v) taken[v] = 0;
+      int r = 0;
+      for (int i = par + 1; i < N; ++i) {
+        if (parents[i] != par) continue;
+        int best = -1;
+        if (!bad && r < V) {
+          /* the r-th largest: the largest logit not taken yet, smallest index on ties */
+          for (int v = 0; v < V; ++v)
+            if (!taken[v] && (best < 0 || z[v] > z[best])) best = v;
+          if (best >= 0) taken[best] = 1;
+        }
+        tok[i] = best;
+        lq[i] = best < 0 ? NAN : log(p[best]);
+        ++r;
+      }
+    }
+  }
+  free(z); free(p); free(taken);
+  return 0;
+}

@@ -304,6 +304,19 @@ def config_kv_commit(B: int = 256, K: int = 5, E: int = 65536, Lmax: int = 64, a
     return KvBatch(n, Lmax, N, E, cache, lengths, scratch, count)
 
 
+def config_tree_draft(B: int = 128, V: int = 128256, branching=(4, 3, 2, 1), N: int = 64,
+                      seed: int = 52_900, seqs=None, dtype: str = BF16):
+    """Top-k tree drafting: draft logit rows ~ N(0,1), one per node of the static
+    BFS tree ``branching`` truncated to N nodes (row p: the draft's distribution
+    for the children of node p).  Returns (parents [N], draft [B, N, V])."""
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    par = bfs_tree(branching, N)
+    draft = np.empty((len(seqs), len(par), V), dtype=np.uint16 if dtype == BF16 else np.float32)
+    for i, b in enumerate(seqs):
+        draft[i] = _store(_rng(seed, b).standard_normal((len(par), V)), dtype)
+    return par, draft
+
+
 def bfs_tree(branching, max_nodes=None) -> np.ndarray:
     """Parent array of a static tree in breadth-first order: the root, then
     ``branching[0]`` children of the root, then ``branching[1]`` children of
@@ -362,5 +375,5 @@ __all__ = [
     "F32", "BF16", "ChainBatch", "TreeBatch", "SIGMA_B256_V128K", "config_greedy",
     "f32_to_bf16_bits", "bf16_bits_to_f64", "as_f64", "gaussian_chain",
     "config_tiny", "config_zipf", "config_headline", "config_controlled",
-    "config_tree", "bfs_tree", "tree_depths", "config_tree_masks", "KvBatch", "config_kv_commit",
+    "config_tree", "config_tree_draft", "bfs_tree", "tree_depths", "config_tree_masks", "KvBatch", "config_kv_commit",
 ]

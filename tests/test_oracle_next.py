@@ -167,3 +167,95 @@ def test_row_stats_invalid_rows(orc):
     a, k, tv = orc.row_stats(z, "f32", y, "f32", False, 1.0)
     assert np.isnan(a[0, 1]) and np.isnan(k[1, 0]) and np.isnan(tv[1, 0])
     assert np.isfinite(a[0, 0]) and np.isfinite(a[1, 1])
+
+
+# --- top-k tree drafting ------------------------------------------------------------
+
+def _np_topk(row, k):
+    """Reference order: decreasing logit, smaller index first on ties (numpy lexsort)."""
+    order = np.lexsort((np.arange(len(row)), -row.astype(np.float64)))
+    return order[:k]
+
+
+def test_tree_draft_page_example(orc):
+    """The pages' example tree: root with candidates a, b; c, d under a; e, f
+    under b.  Each node's children are the top-2 of its draft row."""
+    c = CASES["tree_mask_example"]
+    par = np.array(c["parents"], np.int32)
+    V = 6
+    rows = np.full((1, 7, V), -5.0, np.float32)
+    rows[0, 0, [4, 1]] = [3.0, 2.0]        # root: a = token 4, b = token 1
+    rows[0, 1, [0, 5]] = [1.0, 0.5]        # under a: c = 0, d = 5
+    rows[0, 2, [2, 3]] = [0.25, 0.25]      # under b: a tie, the smaller index first: e = 2, f = 3
+    tok, lq, rc = orc.tree_draft(rows, "f32", par, 1.0)
+    assert rc == 0
+    assert tok[0].tolist() == [-1, 4, 1, 0, 5, 2, 3]
+    from scipy.special import log_softmax
+    ls = log_softmax(rows[0].astype(np.float64), axis=-1)
+    assert lq[0, 0] == 0.0
+    for i in range(1, 7):
+        assert lq[0, i] == pytest.approx(ls[par[i], tok[0, i]], abs=1e-12)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tree_draft_matches_numpy_topk(orc, dtype):
+    rng = np.random.default_rng(21)
+    par = gen.bfs_tree([4, 3, 2, 1], 64)
+    B, N, V, T = 3, len(par), 500, 0.7
+    z = rng.standard_normal((B, N, V))
+    z = np.round(z * 4) / 4                   # many exact ties
+    raw = gen._store(z, dtype) if dtype == "bf16" else z.astype(np.float32)
+    tok, lq, rc = orc.tree_draft(raw, dtype, par, T)
+    zz = gen.as_f64(raw, dtype)
+    from scipy.special import log_softmax
+    for b in range(B):
+        for p in range(N):
+            kids = [i for i in range(N) if par[i] == p]
+            if not kids:
+                continue
+            want = _np_topk(zz[b, p], len(kids))
+            assert tok[b, kids].tolist() == want.tolist()
+            np.testing.assert_allclose(lq[b, kids], log_softmax(zz[b, p] / T)[want], atol=1e-12)
+
+
+def test_tree_draft_chain_is_greedy_and_perfect_draft_is_accepted(orc):
+    """A chain tree drafts the argmax at every step; with the target equal to
+    the draft, greedy tree verification accepts the whole tree depth along the
+    first children."""
+    rng = np.random.default_rng(22)
+    V = 300
+    chain = np.arange(-1, 5, dtype=np.int32)
+    z = rng.standard_normal((2, 6, V)).astype(np.float32)
+    tok, _, _ = orc.tree_draft(z, "f32", chain, 1.0)
+    for b in range(2):
+        assert tok[b, 1:].tolist() == [int(np.argmax(z[b, t])) for t in range(5)]
+    par = gen.bfs_tree([3, 3, 2], None)
+    N = len(par)
+    z = rng.standard_normal((4, N, V)).astype(np.float32)
+    tok, _, _ = orc.tree_draft(z, "f32", par, 1.0)
+    depth = gen.tree_depths(par)
+    out, n, path = orc.verify_tree_greedy(z, "f32", par, tok, int(depth.max()))
+    assert (n == depth.max()).all()
+    first_child = {p: min(i for i in range(N) if par[i] == p) for p in set(par[1:].tolist())}
+    for b in range(4):
+        node = 0
+        for d in range(int(depth.max())):
+            node = first_child[node]
+            assert path[b, d] == node
+
+
+def test_tree_draft_invalid_rows_and_topology(orc):
+    par = np.array([-1, 0, 0, 1, 1], np.int32)
+    z = np.zeros((2, 5, 8), np.float32)
+    z[0, 1, 3] = np.nan                       # node 1's row: its children get -1
+    z[1, 0, :] = -np.inf                      # root row with no finite entry
+    tok, lq, rc = orc.tree_draft(z, "f32", par, 1.0)
+    assert rc == 0
+    assert tok[0, 3] == -1 and tok[0, 4] == -1 and np.isnan(lq[0, 3])
+    assert tok[0, 1] == 0 and tok[0, 2] == 1   # all-equal row: indices in order
+    assert tok[1, 1] == -1 and tok[1, 2] == -1
+    tok, lq, rc = orc.tree_draft(z, "f32", np.array([-1, 0, 2, 1, 1], np.int32), 1.0)
+    assert rc == 1 and (tok == -1).all() and np.isnan(lq).all()
+    tiny = np.zeros((1, 4, 2), np.float32)   # 3 children, V = 2: the third gets -1
+    tok, lq, _ = orc.tree_draft(tiny, "f32", np.array([-1, 0, 0, 0], np.int32), 1.0)
+    assert tok[0].tolist() == [-1, 0, 1, -1] and np.isnan(lq[0, 3])
