@@ -15,6 +15,7 @@ Other workloads (--workload):
   treemask  spec_tree_mask, 4096 per-sequence trees of 256 nodes
   kvcommit  spec_kv_commit, 256 chains, 64 KB entries
   stats     spec_row_stats over the default workload's rows: sum min(p,q), KL, TV
+  draft     spec_tree_draft, B=128 trees of 64 nodes, V=128256: top-k children per node
 Both read only the rows the greedy rules need (rows up to the first mismatch;
 accepted tree nodes), one persistent kernel per call; their algorithmic bytes
 are those rows, counted from the generator's own copy draws.
@@ -33,7 +34,7 @@ region, the SM clocks seen during the run, and the double-precision CPU
 oracle timed on a bounded sample on this host.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload sample|greedy|tree|treemask|kvcommit|stats]
+                    [--workload sample|greedy|tree|treemask|kvcommit|stats|draft]
 """
 from __future__ import annotations
 
@@ -547,8 +548,65 @@ class StatsWorkload(Workload):
         return hs, ds, step, outs
 
 
+class DraftWorkload(Workload):
+    name = "draft"
+    metric = "drafted tree nodes/s"
+    unit = "nodes/s"
+    summary = "tree_draft_kernel_b128_n64_v128256_bf16.md"
+    kernel = "tree_draft_kernel<bf16, 4>"
+    sources = ("common.cuh", "tree_draft.cuh")
+    per_rank = TREE_B
+
+    def describe(self):
+        return {"workload": "top-k tree drafting, B=128 trees of N=64 nodes (BFS [4,3,2,1] truncated), one draft "
+                            "row per node, V=128256 bf16, T=0.7: each node's children take its row's top tokens",
+                "B": TREE_B, "N": TREE_N, "V": V, "temperature": T, "max_children": 4,
+                "l2": "rows read (1.35 GB) larger than L2; no flush"}
+
+    def batch(self, seqs):
+        from speculative_decoding_verification_52_gb300 import inputs as gen
+        par, draft = gen.config_tree_draft(seqs=seqs)
+
+        class _B:
+            pass
+        b = _B()
+        b.B, b.N, b.parents, b.draft = draft.shape[0], draft.shape[1], par, draft
+        return b
+
+    def units(self, batch):
+        return batch.B * (batch.N - 1)
+
+    def algorithmic_bytes(self, batch):
+        import numpy as np
+        internal = len(set(np.asarray(batch.parents[1:]).tolist()))
+        return batch.B * internal * V * 2
+
+    def oracle_chunk(self):
+        return 1
+
+    def oracle_call(self, batch, sl):
+        import numpy as np
+
+        import oracle
+        oracle.tree_draft(np.ascontiguousarray(batch.draft[sl]), "bf16", batch.parents, T, 4)
+
+    def device_setup(self, batch, dev):
+        import torch
+
+        import speculative_decoding_verification_52_gb300 as sv
+        hs = [_bf16_host(batch.draft), _pinned(batch.parents)]
+        ds = [h.to(dev) for h in hs]
+        tok = torch.empty((batch.B, batch.N), dtype=torch.int32, device=dev)
+        lq = torch.empty((batch.B, batch.N), dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream()
+
+        def step():
+            sv.spec_tree_draft(ds[0], ds[1], T, 4, node_tokens=tok, node_logq=lq, stream=stream)
+        return hs, ds, step, [tok, lq]
+
+
 WORKLOADS = {w.name: w for w in (SampleWorkload(), GreedyWorkload(), TreeWorkload(), TreeMaskWorkload(),
-                                 KvCommitWorkload(), StatsWorkload())}
+                                 KvCommitWorkload(), StatsWorkload(), DraftWorkload())}
 
 
 def oracle_rate(wl: Workload, batch, budget_s: float, min_seqs: int):

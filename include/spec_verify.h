@@ -247,6 +247,33 @@ spec_status_t spec_row_stats(const void *target_logits, spec_dtype_t target_dtyp
                              spec_dtype_t draft_dtype, spec_draft_kind_t draft_kind, float temperature, int B,
                              int K, int V, float *alpha, float *kl, float *tv, void *stream);
 
+/* Top-k tree drafting ("Speculative decoding and EAGLE", section "Make it": an
+ * EAGLE-style drafter builds a candidate tree whose branches are the top-k
+ * tokens at each node; exercise 4: the top-3 branches at each depth instead of
+ * a chain).  The step that selects the tree's tokens from the draft's logits,
+ * without the draft model.
+ *
+ *   draft_logits [B, N, V] (draft_dtype): one draft row per tree node; row p is
+ *       the draft's distribution for the token after node p (rows of leaves are
+ *       not read).
+ *   parents [N] int32 (device): parents[0] = -1, 0 <= parents[i] < i.
+ *   max_children: 1..16, the most children any node has (it sizes the
+ *       per-thread candidate lists).
+ *   temperature: > 0; only the log-probabilities depend on it.
+ *   node_tokens [B, N] int32 (device, written): the children of node p, in
+ *       increasing node index, take the tokens of row p in decreasing logit
+ *       order (equal logits: the smaller index first); node 0 gets -1.
+ *   node_logq [B, N] float32 (device, written): log q(token) with
+ *       q = softmax(row p / T) for each child; 0 for node 0.
+ * The children of an invalid row (NaN, +inf, or no finite entry) get -1 and
+ * NaN, as do children whose rank is >= V.  A malformed topology, or a node with
+ * more than max_children children, gives -1 / NaN for every node.
+ * node_tokens and parents can be passed on to spec_tree_mask and
+ * spec_verify_tree_greedy.  Limits: N <= 1024. */
+spec_status_t spec_tree_draft(const void *draft_logits, spec_dtype_t draft_dtype, const int32_t *parents, int B,
+                              int N, int V, int max_children, float temperature, int32_t *node_tokens,
+                              float *node_logq, void *stream);
+
 /* Timing hooks for benchmarks: while enabled, each verify call records CUDA
  * events on the call's stream around its kernels (at most max_calls calls are
  * recorded).  spec_profile_end synchronises on the recorded events and returns

@@ -75,7 +75,7 @@ def lib() -> ctypes.CDLL:
             L.orc_row_stats.argtypes = [P, I, P, I, I, D, I, I, I, P, P, P]
             L.orc_row_stats.restype = I
             L.orc_verify_tree_greedy.restype = I
-            L.orc_tree_draft.argtypes = [P, I, P, I, I, I, D, P, P]
+            L.orc_tree_draft.argtypes = [P, I, P, I, I, I, D, I, P, P]
             L.orc_tree_draft.restype = I
             _lib = L
     return _lib
@@ -266,15 +266,16 @@ def row_stats(target, target_dtype, draft, draft_dtype, draft_is_probs, T: float
     return tuple(out)
 
 
-def tree_draft(draft, dtype, parents, T: float):
+def tree_draft(draft, dtype, parents, T: float, max_children: int = 16):
     """Top-k tree drafting: (node_tokens [B, N] int32, node_logq [B, N] f64, rc);
-    rc = 1 for a malformed topology."""
+    rc = 1 for a malformed topology or a node with more than max_children children."""
     d = _raw(draft, dtype)
     B, N, V = d.shape
     par = np.ascontiguousarray(parents, dtype=np.int32)
     tok = np.empty((B, N), np.int32)
     lq = np.empty((B, N), np.float64)
-    rc = lib().orc_tree_draft(_ptr(d), _dt(dtype), _ptr(par), B, N, V, float(T), _ptr(tok), _ptr(lq))
+    rc = lib().orc_tree_draft(_ptr(d), _dt(dtype), _ptr(par), B, N, V, float(T), int(max_children), _ptr(tok),
+                               _ptr(lq))
     if rc == 2:
         raise MemoryError("oracle allocation failed")
     return tok, lq, rc

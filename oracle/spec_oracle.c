@@ -511,13 +511,20 @@ int orc_row_stats(const void *target, int target_dtype, const void *draft, int d
  * node_logq[b, i] = log q(token) with q = softmax(row p / T), the draft
  * probability of the child's token.  Node 0 gets token -1 and log q 0.  A
  * child whose rank is >= V gets -1 / NaN; so do the children of an invalid row
- * (NaN, +inf, or no finite entry).  A malformed topology gives -1 / NaN for
+ * (NaN, +inf, or no finite entry).  A malformed topology (or a node with more
+ * than max_children children, the caller's stated bound) gives -1 / NaN for
  * every node of every sequence and returns 1. */
 int orc_tree_draft(const void *draft, int dtype, const int32_t *parents, int B, int N, int V, double T,
-                   int32_t *node_tokens, double *node_logq) {
+                   int max_children, int32_t *node_tokens, double *node_logq) {
   int ok = (N >= 1 && parents[0] == -1);
   for (int i = 1; ok && i < N; ++i)
     if (parents[i] < 0 || parents[i] >= i) ok = 0;
+  for (int par = 0; ok && par < N; ++par) {   /* the caller's bound on children per node */
+    int nchild = 0;
+    for (int i = par + 1; i < N; ++i)
+      if (parents[i] == par) ++nchild;
+    if (nchild > max_children) ok = 0;
+  }
   if (!ok) {
     for (size_t k = 0; k < (size_t)B * N; ++k) { node_tokens[k] = -1; node_logq[k] = NAN; }
     return 1;

@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
             L.spec_kv_commit.restype = I
             L.spec_row_stats.argtypes = [P, I, P, I, I, F, I, I, I, P, P, P, P]
             L.spec_row_stats.restype = I
+            L.spec_tree_draft.argtypes = [P, I, P, I, I, I, I, F, P, P, P]
+            L.spec_tree_draft.restype = I
             L.spec_profile_begin.argtypes = [I]
             L.spec_profile_begin.restype = I
             L.spec_profile_end.argtypes = [P, P, P]
@@ -314,6 +316,26 @@ def spec_row_stats(target_logits, draft, temperature, *, draft_kind: str = "logi
                               _stream(stream))
     _check("spec_row_stats", st)
     return tuple(outs)
+
+
+def spec_tree_draft(draft_logits, parents, temperature, max_children: int, *, node_tokens=None, node_logq=None,
+                    stream=None):
+    """Top-k tree drafting.  draft_logits [B,N,V] (bf16/f32), parents [N] int32.
+    Returns (node_tokens [B,N] int32, node_logq [B,N] f32)."""
+    _dev(draft_logits, "draft_logits")
+    _dev(parents, "parents")
+    B, N, V = draft_logits.shape
+    if node_tokens is None:
+        node_tokens = torch.empty((B, N), dtype=torch.int32, device=draft_logits.device)
+    if node_logq is None:
+        node_logq = torch.empty((B, N), dtype=torch.float32, device=draft_logits.device)
+    _dev(node_tokens, "node_tokens")
+    _dev(node_logq, "node_logq")
+    st = lib().spec_tree_draft(_ptr(draft_logits), _dtype_code(draft_logits), _ptr(parents), B, N, V,
+                               int(max_children), float(temperature), _ptr(node_tokens), _ptr(node_logq),
+                               _stream(stream))
+    _check("spec_tree_draft", st)
+    return node_tokens, node_logq
 
 
 def spec_profile_begin(max_calls: int):

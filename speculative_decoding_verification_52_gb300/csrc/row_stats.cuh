@@ -138,6 +138,8 @@ __global__ void __launch_bounds__(RS_THREADS) row_stats_kernel(RowStatsArgs a) {
   __shared__ int s_timeout;
 
   const uint32_t CS = static_cast<uint32_t>(a.CS);
+  // bf16 target and draft logits: packed bf16x2 / f32x2 arithmetic
+  constexpr bool kPackedBF16 = TP::esz == 2 && TQ::esz == 2 && !PROBS;
   const uint32_t rank = cluster_rank();
   const long long pos = blockIdx.x / CS;   // (sequence, position) pair of this cluster
   const int b = static_cast<int>(pos / a.K), t = static_cast<int>(pos % a.K);
@@ -195,15 +197,27 @@ __global__ void __launch_bounds__(RS_THREADS) row_stats_kernel(RowStatsArgs a) {
   // ---- pass A: row maxima ----------------------------------------------------
   float mx[2] = {kNegInf, kNegInf};
   {
-    float zp[8], zq[8];
-    for (int g = threadIdx.x; g < ng; g += RS_THREADS) {
-      rs_ld8<TP>(sp, g, zp);
+    if constexpr (kPackedBF16) {
+      // NaN-propagating packed maxima of the raw bf16 words, halves combined once
+      uint32_t mp = 0xff80ff80u, mq = 0xff80ff80u;
+      for (int g = threadIdx.x; g < ng; g += RS_THREADS) {
+        const uint4 a4 = reinterpret_cast<const uint4*>(sp)[g], b4 = reinterpret_cast<const uint4*>(sq)[g];
+        mp = bf16x2_max_nan(mp, bf16x2_max_nan(bf16x2_max_nan(a4.x, a4.y), bf16x2_max_nan(a4.z, a4.w)));
+        mq = bf16x2_max_nan(mq, bf16x2_max_nan(bf16x2_max_nan(b4.x, b4.y), bf16x2_max_nan(b4.z, b4.w)));
+      }
+      mx[0] = fmax_nan(__uint_as_float(mp << 16), __uint_as_float(mp & 0xffff0000u));
+      mx[1] = fmax_nan(__uint_as_float(mq << 16), __uint_as_float(mq & 0xffff0000u));
+    } else {
+      float zp[8], zq[8];
+      for (int g = threadIdx.x; g < ng; g += RS_THREADS) {
+        rs_ld8<TP>(sp, g, zp);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[0] = fmax_nan(mx[0], zp[i]);
-      if (!PROBS) {
-        rs_ld8<TQ>(sq, g, zq);
+        for (int i = 0; i < 8; ++i) mx[0] = fmax_nan(mx[0], zp[i]);
+        if (!PROBS) {
+          rs_ld8<TQ>(sq, g, zq);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[1] = fmax_nan(mx[1], zq[i]);
+          for (int i = 0; i < 8; ++i) mx[1] = fmax_nan(mx[1], zq[i]);
+        }
       }
     }
   }
@@ -226,7 +240,38 @@ __global__ void __launch_bounds__(RS_THREADS) row_stats_kernel(RowStatsArgs a) {
 
   // ---- pass B: normalisers ---------------------------------------------------
   float vb[4] = {0.f, 0.f, 0.f, 0.f};
-  {
+  if constexpr (kPackedBF16) {
+    // per pair of elements: both exponents by one packed fma each, two ex2
+    // per row, D += e_q (y - z) with y - z >= -FLT_MAX (a -inf draft logit has
+    // e_q = 0 and must add nothing)
+    const unsigned long long c2 = f2_pack(c, c), kp2 = f2_pack(kp, kp), kq2 = f2_pack(kq, kq);
+    const unsigned long long m1 = f2_pack(-1.f, -1.f);
+    unsigned long long sp2 = f2_pack(0.f, 0.f), sq2 = sp2, d2 = sp2;
+    for (int g = threadIdx.x; g < ng; g += RS_THREADS) {
+      const uint4 a4 = reinterpret_cast<const uint4*>(sp)[g], b4 = reinterpret_cast<const uint4*>(sq)[g];
+      const uint32_t wz[4] = {a4.x, a4.y, a4.z, a4.w}, wy[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const unsigned long long z2 = bf16x2_to_f2(wz[i]), y2 = bf16x2_to_f2(wy[i]);
+        float a0, a1, b0, b1, t0, t1;
+        f2_unpack(f2_fma(z2, c2, kp2), a0, a1);
+        f2_unpack(f2_fma(y2, c2, kq2), b0, b1);
+        const unsigned long long ep2 = f2_pack(ex2_approx(a0), ex2_approx(a1));
+        const unsigned long long eq2 = f2_pack(ex2_approx(b0), ex2_approx(b1));
+        sp2 = f2_add(sp2, ep2);
+        sq2 = f2_add(sq2, eq2);
+        f2_unpack(f2_fma(z2, m1, y2), t0, t1);
+        d2 = f2_fma(eq2, f2_pack(fmaxf(t0, -3.402823466e38f), fmaxf(t1, -3.402823466e38f)), d2);
+      }
+    }
+    float x0, x1;
+    f2_unpack(sp2, x0, x1);
+    vb[0] = x0 + x1;
+    f2_unpack(sq2, x0, x1);
+    vb[1] = x0 + x1;
+    f2_unpack(d2, x0, x1);
+    vb[2] = x0 + x1;
+  } else {
     float zp[8], zq[8];
     for (int g = threadIdx.x; g < ng; g += RS_THREADS) {
       rs_ld8<TP>(sp, g, zp);
@@ -283,7 +328,24 @@ __global__ void __launch_bounds__(RS_THREADS) row_stats_kernel(RowStatsArgs a) {
 
   // ---- pass C: alpha (and, for probabilities, TV and KL) ----------------------
   float vc[3] = {0.f, 0.f, 0.f};
-  {
+  if constexpr (kPackedBF16) {
+    const unsigned long long c2 = f2_pack(c, c), up2 = f2_pack(up, up), uq2 = f2_pack(uq, uq);
+    unsigned long long al2 = f2_pack(0.f, 0.f);
+    for (int g = threadIdx.x; g < ng; g += RS_THREADS) {
+      const uint4 a4 = reinterpret_cast<const uint4*>(sp)[g], b4 = reinterpret_cast<const uint4*>(sq)[g];
+      const uint32_t wz[4] = {a4.x, a4.y, a4.z, a4.w}, wy[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float a0, a1, b0, b1;
+        f2_unpack(f2_fma(bf16x2_to_f2(wz[i]), c2, up2), a0, a1);
+        f2_unpack(f2_fma(bf16x2_to_f2(wy[i]), c2, uq2), b0, b1);
+        al2 = f2_add(al2, f2_pack(ex2_approx(fminf(a0, b0)), ex2_approx(fminf(a1, b1))));
+      }
+    }
+    float x0, x1;
+    f2_unpack(al2, x0, x1);
+    vc[0] = x0 + x1;
+  } else {
     float zp[8], zq[8];
     for (int g = threadIdx.x; g < ng; g += RS_THREADS) {
       rs_ld8<TP>(sp, g, zp);

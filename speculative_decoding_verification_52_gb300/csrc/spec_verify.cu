@@ -28,6 +28,7 @@
 #include "tree_mask.cuh"
 #include "kv_commit.cuh"
 #include "row_stats.cuh"
+#include "tree_draft.cuh"
 
 namespace {
 
@@ -661,6 +662,21 @@ spec_status_t launch_row_stats(int dev, const RowStatsArgs& a, cudaStream_t st) 
   return SPEC_OK;
 }
 
+// ---------------------------------------------------------------------------
+// top-k tree drafting
+// ---------------------------------------------------------------------------
+template <class T, int KM>
+spec_status_t launch_tree_draft(int dev, unsigned grid, size_t smem, const TreeDraftArgs& a, cudaStream_t st) {
+  auto kern = tree_draft_kernel<T, KM>;
+  if (!once_per_device(dev, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TD_NS * TD_STAGE) ==
+               cudaSuccess;
+      }))
+    return fail(SPEC_ERR_CUDA, "tree draft kernel setup failed: %s", cudaGetErrorString(cudaGetLastError()));
+  kern<<<grid, TD_THREADS, smem, st>>>(a);
+  return SPEC_OK;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -995,6 +1011,71 @@ spec_status_t spec_row_stats(const void* target_logits, spec_dtype_t target_dtyp
       s = draft_dtype == SPEC_BF16 ? launch_row_stats<F32T, BF16T, false>(dev, a, st)
                                    : launch_row_stats<F32T, F32T, false>(dev, a, st);
     if (s != SPEC_OK) return s;
+    prof_mark(1, st);
+    prof_mark(2, st);
+    return SPEC_OK;
+  } catch (...) {
+    return fail(SPEC_ERR_CUDA, "unexpected host exception");
+  }
+}
+
+spec_status_t spec_tree_draft(const void* draft_logits, spec_dtype_t draft_dtype, const int32_t* parents, int B,
+                              int N, int V, int max_children, float temperature, int32_t* node_tokens,
+                              float* node_logq, void* stream) {
+  try {
+    if (B < 0 || N < 1 || N > TD_MAX_N || V < 1)
+      return fail(SPEC_ERR_INVALID_ARG, "bad sizes B=%d N=%d V=%d (N in [1, %d])", B, N, V, TD_MAX_N);
+    if (max_children < 1 || max_children > TD_MAX_CHILDREN)
+      return fail(SPEC_ERR_INVALID_ARG, "max_children=%d outside [1, %d]", max_children, TD_MAX_CHILDREN);
+    if (!dtype_ok(draft_dtype)) return fail(SPEC_ERR_INVALID_ARG, "bad dtype");
+    if (!(temperature > 0.f) || !std::isfinite(temperature))
+      return fail(SPEC_ERR_INVALID_ARG, "temperature must be > 0 and finite");
+    if (temperature < 1e-4f) return fail(SPEC_ERR_UNSUPPORTED, "temperature %g below 1e-4", temperature);
+    if (static_cast<long long>(B) * N > 0x7fffffffLL) return fail(SPEC_ERR_UNSUPPORTED, "grid too large");
+    if (B == 0) return SPEC_OK;
+    if (!draft_logits || !parents || !node_tokens || !node_logq)
+      return fail(SPEC_ERR_INVALID_ARG, "NULL draft/parents/node_tokens/node_logq");
+    int dev;
+    DevInfo di;
+    spec_status_t s = device_info(di, dev);
+    if (s != SPEC_OK) return s;
+    TreeDraftArgs a{};
+    a.draft = static_cast<const unsigned char*>(draft_logits);
+    a.parents = parents;
+    a.B = B;
+    a.N = N;
+    a.V = V;
+    a.max_children = max_children;
+    const int esz = esz_of(draft_dtype);
+    a.vec = aligned16(draft_logits) && (static_cast<long long>(V) * esz) % 16 == 0;
+    a.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+    a.node_tokens = node_tokens;
+    a.node_logq = node_logq;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const unsigned grid = static_cast<unsigned>(static_cast<long long>(B) * N);
+    prof_mark(0, st);
+    const int km = max_children <= 1 ? 1 : max_children <= 2 ? 2 : max_children <= 4 ? 4 : max_children <= 8 ? 8 : 16;
+    const size_t smem = a.vec ? static_cast<size_t>(TD_NS) * TD_STAGE : 0;
+    if (draft_dtype == SPEC_BF16) {
+      switch (km) {
+        case 1: s = launch_tree_draft<BF16T, 1>(dev, grid, smem, a, st); break;
+        case 2: s = launch_tree_draft<BF16T, 2>(dev, grid, smem, a, st); break;
+        case 4: s = launch_tree_draft<BF16T, 4>(dev, grid, smem, a, st); break;
+        case 8: s = launch_tree_draft<BF16T, 8>(dev, grid, smem, a, st); break;
+        default: s = launch_tree_draft<BF16T, 16>(dev, grid, smem, a, st); break;
+      }
+    } else {
+      switch (km) {
+        case 1: s = launch_tree_draft<F32T, 1>(dev, grid, smem, a, st); break;
+        case 2: s = launch_tree_draft<F32T, 2>(dev, grid, smem, a, st); break;
+        case 4: s = launch_tree_draft<F32T, 4>(dev, grid, smem, a, st); break;
+        case 8: s = launch_tree_draft<F32T, 8>(dev, grid, smem, a, st); break;
+        default: s = launch_tree_draft<F32T, 16>(dev, grid, smem, a, st); break;
+      }
+    }
+    if (s != SPEC_OK) return s;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "tree draft launch");
     prof_mark(1, st);
     prof_mark(2, st);
     return SPEC_OK;

@@ -152,3 +152,18 @@ def test_row_stats_rejects_bad_arguments(L):
     assert call(V=1_000_000) == B.SPEC_ERR_UNSUPPORTED       # slice pair beyond the limit
     assert call(Bn=0, t=None, d=None, a=None) == B.SPEC_OK
     assert call(K=0, t=None, d=None, a=None) == B.SPEC_OK
+
+
+def test_tree_draft_rejects_bad_arguments(L):
+    P, F = ctypes.c_void_p, ctypes.c_float
+    td = L.spec_tree_draft
+    assert td(P(16), B.SPEC_BF16, P(32), 2, 0, 64, 4, F(1.0), P(48), P(64), None) == B.SPEC_ERR_INVALID_ARG
+    assert td(P(16), B.SPEC_BF16, P(32), 2, 1025, 64, 4, F(1.0), P(48), P(64), None) == B.SPEC_ERR_INVALID_ARG
+    assert td(P(16), B.SPEC_BF16, P(32), 2, 8, 0, 4, F(1.0), P(48), P(64), None) == B.SPEC_ERR_INVALID_ARG
+    assert td(P(16), B.SPEC_BF16, P(32), 2, 8, 64, 0, F(1.0), P(48), P(64), None) == B.SPEC_ERR_INVALID_ARG
+    assert td(P(16), B.SPEC_BF16, P(32), 2, 8, 64, 17, F(1.0), P(48), P(64), None) == B.SPEC_ERR_INVALID_ARG
+    assert td(P(16), B.SPEC_BF16, P(32), 2, 8, 64, 4, F(0.0), P(48), P(64), None) == B.SPEC_ERR_INVALID_ARG
+    assert td(P(16), B.SPEC_BF16, P(32), 2, 8, 64, 4, F(1e-6), P(48), P(64), None) == B.SPEC_ERR_UNSUPPORTED
+    assert td(P(16), 9, P(32), 2, 8, 64, 4, F(1.0), P(48), P(64), None) == B.SPEC_ERR_INVALID_ARG
+    assert td(P(16), B.SPEC_BF16, None, 2, 8, 64, 4, F(1.0), P(48), P(64), None) == B.SPEC_ERR_INVALID_ARG
+    assert td(None, B.SPEC_BF16, None, 0, 8, 64, 4, F(1.0), None, None, None) == B.SPEC_OK

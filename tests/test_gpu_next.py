@@ -190,3 +190,104 @@ def test_row_stats_empty():
     d = torch.zeros((3, 0, 64), dtype=torch.bfloat16, device=gu.DEV)
     a, k, tv = sv.spec_row_stats(t, d, 1.0)
     assert a.shape == (3, 0)
+
+
+# --- top-k tree drafting ------------------------------------------------------------
+# Tokens are compared bit for bit (the selection compares logits exactly).  log q
+# = ln2 (z c - fl(M c) - log2 S) in fp32: log2 S (|.| <= ~20) and the final
+# difference carry ~1 ulp of ~20 each, ~4e-6 in all, so 2e-5 absolute.
+LOGQ_ATOL = 2e-5
+
+
+def _draft_pair(orc, draft, dtype, parents, T, max_children):
+    tok, lq = sv.spec_tree_draft(gu.dev_tensor(draft, dtype), gu.i32(parents), T, max_children)
+    tok, lq = tok.cpu().numpy(), lq.cpu().numpy().astype(np.float64)
+    rt, rl, _ = orc.tree_draft(draft, dtype, parents, T, max_children)
+    np.testing.assert_array_equal(tok, rt)
+    np.testing.assert_array_equal(np.isnan(lq), np.isnan(rl))
+    ok = ~np.isnan(rl)
+    np.testing.assert_allclose(lq[ok], rl[ok], rtol=1e-6, atol=LOGQ_ATOL)
+    return tok, lq
+
+
+@pytest.mark.parametrize("dtype,V,branching,N,mc", [
+    ("bf16", 128256, (4, 3, 2, 1), 64, 4),
+    ("f32", 32000, (3, 3, 2), None, 3),
+    ("bf16", 999, (4, 3, 2, 1), 64, 4),      # rows not 16-byte aligned: element loads
+    ("f32", 37, (1, 1, 1, 1, 1), None, 1),   # a chain: the argmax at every step
+    ("bf16", 4096, (16, 2), None, 16),
+    ("f32", 5000, (2, 2, 2, 2, 2, 2), None, 8),
+])
+def test_tree_draft_matches_oracle(orc, dtype, V, branching, N, mc):
+    par, draft = gen.config_tree_draft(B=5, V=V, branching=branching, N=N, dtype=dtype, seed=52_910 + V)
+    _draft_pair(orc, draft, dtype, par, 0.8, mc)
+
+
+def test_tree_draft_ties_and_small_vocab(orc):
+    rng = np.random.default_rng(7)
+    par = gen.bfs_tree([5, 2], None)
+    z = (np.round(rng.standard_normal((6, len(par), 700)) * 2) / 2).astype(np.float32)   # many exact ties
+    _draft_pair(orc, z, "f32", par, 1.0, 5)
+    _draft_pair(orc, gen._store(z.astype(np.float64), "bf16"), "bf16", par, 1.3, 8)
+    tiny = rng.standard_normal((3, 4, 2)).astype(np.float32)          # 3 children, V = 2
+    _draft_pair(orc, tiny, "f32", np.array([-1, 0, 0, 0], np.int32), 1.0, 3)
+
+
+def test_tree_draft_invalid_rows_and_topology(orc):
+    par = gen.bfs_tree([3, 2], None)
+    rng = np.random.default_rng(8)
+    z = rng.standard_normal((4, len(par), 256)).astype(np.float32)
+    z[0, 1, 7] = np.nan
+    z[1, 0, :] = -np.inf
+    z[2, 2, 5] = np.inf
+    _draft_pair(orc, z, "f32", par, 1.0, 3)
+    bad = par.copy()
+    bad[4] = 6                                           # a parent after its child
+    tok, lq = _draft_pair(orc, z, "f32", bad, 1.0, 3)
+    assert (tok == -1).all()
+    tok, _ = _draft_pair(orc, z, "f32", par, 1.0, 2)     # the root has 3 children > 2
+    assert (tok == -1).all()
+
+
+def test_tree_draft_full_workload_sampled(orc):
+    """B=128, N=64, V=128256 bf16 in the benchmark's launch configuration; every
+    8th sequence against the oracle."""
+    par, draft = gen.config_tree_draft()
+    tok, lq = sv.spec_tree_draft(gu.dev_tensor(draft, "bf16"), gu.i32(par), 0.7, 4)
+    tok, lq = tok.cpu().numpy(), lq.cpu().numpy().astype(np.float64)
+    sel = np.arange(0, 128, 8)
+    rt, rl, _ = orc.tree_draft(np.ascontiguousarray(draft[sel]), "bf16", par, 0.7, 4)
+    np.testing.assert_array_equal(tok[sel], rt)
+    np.testing.assert_allclose(lq[sel], rl, rtol=1e-6, atol=LOGQ_ATOL)
+
+
+def test_draft_mask_verify_pipeline(orc):
+    """Draft a tree, build its attention mask, verify it: a target equal to the
+    draft accepts the whole depth along the first children; a target whose
+    root row prefers the root's second token accepts through the second child."""
+    par, draft = gen.config_tree_draft(B=6, V=8192, seed=52_920)
+    d = gu.dev_tensor(draft, "bf16")
+    ptr = gu.i32(par)
+    tok, _ = sv.spec_tree_draft(d, ptr, 1.0, 4)
+    masks, st = sv.spec_tree_mask(ptr)
+    rm, _ = orc.tree_mask(par)
+    np.testing.assert_array_equal(masks.cpu().numpy().view(np.uint32)[0], rm[0])
+    depth = gen.tree_depths(par)
+    out, n, path = sv.spec_verify_tree_greedy(d, ptr, tok, int(depth.max()))
+    assert (n.cpu().numpy() == depth.max()).all()
+    first = {p: min(i for i in range(len(par)) if par[i] == p) for p in set(par[1:].tolist())}
+    node = 0
+    for dd in range(int(depth.max())):
+        node = first[node]
+        assert (path.cpu().numpy()[:, dd] == node).all()
+    # a target whose root row ranks the root's second child's token first
+    t = draft.copy()
+    tnp = tok.cpu().numpy()
+    for b in range(6):
+        row = gen.as_f64(t[b, 0], "bf16")
+        row[tnp[b, 2]] = row.max() + 1.0
+        t[b, 0] = gen._store(row, "bf16")
+    out, n, path = sv.spec_verify_tree_greedy(gu.dev_tensor(t, "bf16"), ptr, tok, int(depth.max()))
+    ro, rn, rp = orc.verify_tree_greedy(t, "bf16", par, tnp, int(depth.max()))
+    np.testing.assert_array_equal(path.cpu().numpy(), rp)
+    assert (rp[:, 0] == 2).all()

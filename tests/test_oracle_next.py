@@ -256,6 +256,8 @@ def test_tree_draft_invalid_rows_and_topology(orc):
     assert tok[1, 1] == -1 and tok[1, 2] == -1
     tok, lq, rc = orc.tree_draft(z, "f32", np.array([-1, 0, 2, 1, 1], np.int32), 1.0)
     assert rc == 1 and (tok == -1).all() and np.isnan(lq).all()
+    tok, lq, rc = orc.tree_draft(z, "f32", par, 1.0, max_children=1)   # the root has 2 children
+    assert rc == 1 and (tok == -1).all() and np.isnan(lq).all()
     tiny = np.zeros((1, 4, 2), np.float32)   # 3 children, V = 2: the third gets -1
     tok, lq, _ = orc.tree_draft(tiny, "f32", np.array([-1, 0, 0, 0], np.int32), 1.0)
     assert tok[0].tolist() == [-1, 0, 1, -1] and np.isnan(lq[0, 3])
