@@ -183,6 +183,19 @@ spec_status_t spec_debug_residual(const void *target_logits, spec_dtype_t target
                                   int32_t *out_tokens, int32_t *num_accepted, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
+/* Test hook for the bounded waits (no counterpart on the pages): runs
+ * spec_verify_sample with every device-side wait limited to timeout_us
+ * microseconds (100..1000000) while the accept scan of sequence stall_b waits
+ * for one sweep unit more than the call produces, so that wait runs out.  The
+ * call must end with num_accepted[b] = -2 and out_tokens[b, :] = -1 for every
+ * b, and leave the context and the workspace usable.  Needs the fused
+ * sampling path (T > 0, 16-byte aligned rows); SPEC_ERR_UNSUPPORTED otherwise. */
+spec_status_t spec_debug_stall(const void *target_logits, spec_dtype_t target_dtype, const void *draft,
+                               spec_dtype_t draft_dtype, spec_draft_kind_t draft_kind, const int32_t *draft_tokens,
+                               const float *uniforms, float temperature, int B, int K, int V, int stall_b,
+                               unsigned timeout_us, int32_t *out_tokens, int32_t *num_accepted, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
 /* Tree attention mask ("Speculative decoding and EAGLE", section "Tree
  * attention verification"; "Speculative Decoding: from idea to SOTA",
  * section 6): when the draft proposes a tree, the target scores all of it in

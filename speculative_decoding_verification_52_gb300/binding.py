@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_tree_greedy.restype = I
             L.spec_debug_residual.argtypes = [P, I, P, I, I, P, P, F, I, I, I, I, I, P, P, P, P, P, Z, P]
             L.spec_debug_residual.restype = I
+            L.spec_debug_stall.argtypes = [P, I, P, I, I, P, P, F, I, I, I, I, ctypes.c_uint, P, P, P, Z, P]
+            L.spec_debug_stall.restype = I
             L.spec_tree_mask.argtypes = [P, I, I, P, P, P]
             L.spec_tree_mask.restype = I
             L.spec_kv_commit.argtypes = [P, P, P, P, P, I, I, I, I, Z, P, P]
@@ -255,6 +257,24 @@ def spec_debug_residual(target_logits, draft, draft_tokens, uniforms, temperatur
                                    _ptr(ws), ws.numel(), _stream(stream))
     _check("spec_debug_residual", st)
     return row, mass, out_tokens, num_accepted
+
+
+def spec_debug_stall(target_logits, draft, draft_tokens, uniforms, temperature, stall_b: int, timeout_us: int, *,
+                     stream=None):
+    """Test hook: spec_verify_sample with short wait limits while one
+    sequence's scan waits for a unit that never comes.  Returns
+    (out_tokens, num_accepted); every sequence should read -2."""
+    _dev(target_logits, "target_logits")
+    B, W, V = target_logits.shape
+    K = W - 1
+    out_tokens, num_accepted = _outputs(B, W, target_logits.device, None, None)
+    ws = workspace(spec_workspace_bytes(B, K, V), target_logits.device)
+    st = lib().spec_debug_stall(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), _dtype_code(draft),
+                                SPEC_DRAFT_LOGITS, _ptr(draft_tokens), _ptr(uniforms), float(temperature), B, K, V,
+                                int(stall_b), int(timeout_us), _ptr(out_tokens), _ptr(num_accepted), _ptr(ws),
+                                ws.numel(), _stream(stream))
+    _check("spec_debug_stall", st)
+    return out_tokens, num_accepted
 
 
 def spec_tree_mask(parents, *, masks=None, status=None, stream=None):

@@ -111,6 +111,7 @@ struct FusedArgs {
   int32_t* out_tokens;           // [B, K+1]
   int32_t* num_accepted;         // [B]
   int debug_b, debug_t;
+  int debug_stall_b;             // test hook: this sequence's scan waits for a unit that never comes (-1: off)
   float* debug_row;
   float* debug_mass;
   unsigned long long timeout_ns;
@@ -1090,7 +1091,9 @@ __device__ void fu_finisher(const FusedArgs& a, FuShared& sh, int lane) {
     if (lane == 2 && bp < static_cast<unsigned>(a.B)) v = ld_relaxed_u32(fu_cnt2(a, static_cast<int>(bp)));
     const unsigned v_scan = __shfl_sync(0xffffffffu, v, 1);
     const unsigned v_pick = __shfl_sync(0xffffffffu, v, 2);
-    if (bs < static_cast<unsigned>(a.B) && v_scan == per_seq) {
+    // (the test hook asks one sequence's scan for one unit more than exists)
+    const unsigned need_scan = per_seq + (static_cast<int>(bs) == a.debug_stall_b ? 1u : 0u);
+    if (bs < static_cast<unsigned>(a.B) && v_scan == need_scan) {
       __threadfence();
       finish_scan<TP, TQ, PROBS>(a, static_cast<int>(bs), lane, in);
       bs += G;

@@ -176,6 +176,18 @@ spec_status_t launch_sweep(const DevInfo& di, int dev, bool vec, const unsigned 
 }
 
 // ---------------------------------------------------------------------------
+// test hook of spec_debug_stall: while set (on the calling thread), the fused
+// sampling kernel runs with this wait limit and one sequence's accept scan
+// waits for a sweep unit that never comes
+// ---------------------------------------------------------------------------
+struct StallHook {
+  int b = -1;
+  unsigned long long timeout_ns = 0;
+  bool applied = false;
+};
+thread_local StallHook g_stall;
+
+// ---------------------------------------------------------------------------
 // profiling events
 // ---------------------------------------------------------------------------
 struct Prof {
@@ -396,6 +408,12 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   a.debug_row = debug_row;
   a.debug_mass = debug_mass;
   a.timeout_ns = kWaitNs;
+  a.debug_stall_b = -1;
+  if (g_stall.b >= 0) {   // test hook (spec_debug_stall)
+    a.debug_stall_b = g_stall.b;
+    a.timeout_ns = g_stall.timeout_ns;
+    g_stall.applied = true;
+  }
   cudaError_t e = cudaMemsetAsync(ws, 0, lay.zero_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "workspace control reset");
   prof_mark(0, st);
@@ -1079,6 +1097,33 @@ spec_status_t spec_tree_draft(const void* draft_logits, spec_dtype_t draft_dtype
     prof_mark(1, st);
     prof_mark(2, st);
     return SPEC_OK;
+  } catch (...) {
+    return fail(SPEC_ERR_CUDA, "unexpected host exception");
+  }
+}
+
+spec_status_t spec_debug_stall(const void* target_logits, spec_dtype_t target_dtype, const void* draft,
+                               spec_dtype_t draft_dtype, spec_draft_kind_t draft_kind, const int32_t* draft_tokens,
+                               const float* uniforms, float temperature, int B, int K, int V, int stall_b,
+                               unsigned timeout_us, int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  try {
+    if (stall_b < 0 || stall_b >= B) return fail(SPEC_ERR_INVALID_ARG, "stall_b=%d outside the batch", stall_b);
+    if (timeout_us < 100 || timeout_us > 1000000u)
+      return fail(SPEC_ERR_INVALID_ARG, "timeout_us=%u outside [100, 1000000]", timeout_us);
+    if (!(temperature > 0.f)) return fail(SPEC_ERR_INVALID_ARG, "the stall hook needs the sampling rule (T > 0)");
+    struct Reset {
+      ~Reset() { g_stall = StallHook{}; }
+    } reset;
+    g_stall.b = stall_b;
+    g_stall.timeout_ns = static_cast<unsigned long long>(timeout_us) * 1000ull;
+    g_stall.applied = false;
+    spec_status_t s = sample_entry(target_logits, target_dtype, draft, draft_dtype, draft_kind, draft_tokens,
+                                   uniforms, temperature, B, K, V, out_tokens, num_accepted, workspace,
+                                   workspace_bytes, -1, -1, nullptr, nullptr, stream);
+    if (s == SPEC_OK && !g_stall.applied)
+      return fail(SPEC_ERR_UNSUPPORTED, "the stall hook needs the fused sampling path (16-byte aligned rows)");
+    return s;
   } catch (...) {
     return fail(SPEC_ERR_CUDA, "unexpected host exception");
   }
