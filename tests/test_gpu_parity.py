@@ -140,12 +140,26 @@ def test_sample_headline_full(orc):
     assert 0.4 < acc < 0.95
 
 
-@pytest.mark.parametrize("B,K", [(1, 4), (8, 8), (64, 4), (64, 8)])
+@pytest.mark.parametrize("B,K", [(1, 4), (1, 8), (8, 4), (8, 8), (64, 4), (64, 8)])
 def test_sample_controlled(orc, B, K):
     b = gen.config_controlled(B, K)
     ref = gu.oracle_sample(orc, b)
     out, n = gu.gpu_sample(b)
     gu.compare_sample(out, n, ref)
+
+
+def test_sample_controlled_b512_k8_sampled(orc):
+    """The largest sweep case, B=512, K=8, V=151936 (2.8 GB of logits), in one
+    call; every fourth sequence against the oracle (the generator seeds each
+    sequence on its own, so a subset reproduces the same rows)."""
+    b = gen.config_controlled(512, 8)
+    out, n = gu.gpu_sample(b)
+    sel = list(range(0, 512, 4))
+    sub = gen.config_controlled(512, 8, seqs=sel)
+    ref = gu.oracle_sample(orc, sub)
+    assert (sub.target == b.target[sel]).all()
+    gu.compare_sample(out[sel], n[sel], ref)
+    assert (n >= 0).all()
 
 
 def test_sample_controlled_b512_expected_tokens(orc):
