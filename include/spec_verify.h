@@ -280,7 +280,8 @@ spec_status_t spec_row_stats(const void *target_logits, spec_dtype_t target_dtyp
  *       q = softmax(row p / T) for each child; 0 for node 0.
  * The children of an invalid row (NaN, +inf, or no finite entry) get -1 and
  * NaN, as do children whose rank is >= V.  A malformed topology, or a node with
- * more than max_children children, gives -1 / NaN for every node.
+ * more than max_children children, gives -1 / NaN for every node.  A row
+ * whose copy wait hit its time limit gives its children -2 / NaN.
  * node_tokens and parents can be passed on to spec_tree_mask and
  * spec_verify_tree_greedy.  Limits: N <= 1024. */
 spec_status_t spec_tree_draft(const void *draft_logits, spec_dtype_t draft_dtype, const int32_t *parents, int B,

@@ -7,13 +7,14 @@
 // One CTA per (sequence, node).  The CTA finds the node's children (the nodes
 // whose parent it is, in index order) and checks the topology; a node without
 // children has nothing to draft and leaves.  Otherwise the CTA streams the
-// node's draft row once with 16-byte loads (four in flight per thread) and
-// keeps, per thread,
+// node's draft row once through a ring of shared-memory stages filled by bulk
+// async copies and keeps, per thread,
 //   - the online softmax normaliser (m, sum 2^(z c - fl(m c))), c = log2(e)/T;
 //   - the KM best elements as 64-bit keys (orderable float bits << 32 |
 //     ~index): a larger key is a larger logit, or an equal logit at a smaller
-//     index, so key order is the drafting order.  A vector whose maximum does
-//     not beat the thread's KM-th best is skipped after one compare.
+//     index, so key order is the drafting order.  Elements are offered to the
+//     list only when they reach a bound that no element below it can beat: the
+//     KM-th best key of the warp's lists, or of any warp of the CTA.
 // The lists are merged per warp and then across warps in KM rounds of
 // argmax extraction; child r of the node receives key r.
 #pragma once
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
         // the lanes' group maxima (KM distinct elements reach it, so nothing
         // below it can be in the top KM).  Indices interleave across lanes in
         // this group, so equal values must still be examined: the bound is
-        // lowered by one ulp and the strict tests admit them.
+        // lowered by one ulp, and the bound tests admit equal values anyway.
         float v = vm, kth = kNegInf;
 #pragma unroll
         for (int r = 0; r < KM; ++r) {
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
           const unsigned hit = __ballot_sync(0xffffffffu, v == m);
           if (lane == __ffs(hit) - 1) v = kNegInf;   // one lane per round leaves
         }
-        wbound = kth > kNegInf && KM <= 32;
+        wbound = kth > kNegInf;
         wthr = wbound ? nextafterf(kth, kNegInf) : kNegInf;
       }
       // NaN never passes these filters (bf16x2 max skips it; the sum above
@@ -385,11 +386,12 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
         }
       }
       // The KM-th best key of the union of the warp's lists bounds what can
-      // still enter the warp's (hence the CTA's) top KM.  Later groups hold
-      // larger indices than all elements seen, so an equal value never wins and
-      // the strict tests above are exact; an older bound is lower, hence still
-      // valid, so it is refreshed only every TD_BOUND_EVERY groups.  Until the
-      // warp holds KM keys there is no bound and every group is examined.
+      // still enter the warp's (hence the CTA's) top KM.  The bound tests admit
+      // equal values and the key comparison then orders ties by index, so the
+      // filter never drops a member of the top KM; an older bound is lower,
+      // hence still valid, so it is refreshed only every TD_BOUND_EVERY groups.
+      // Until the warp holds KM keys there is no bound and every group is
+      // examined.
       if ((ch & (TD_BOUND_EVERY - 1)) == 0 || ch < 2) {
         // the exact bound: the KM-th best key the warp holds
         const unsigned long long wk = td_warp_kth<KM>(k);
