@@ -91,7 +91,8 @@ __device__ __forceinline__ void rs_pad(unsigned char* s, int i, bool zero) {
 }
 
 // block-wide reduction of up to 4 values (op: 0 = sum, 1 = NaN-propagating max);
-// every thread receives the result
+// every thread receives the result.  Each call site has its own scratch
+// array, so no barrier is needed before the scratch is written.
 template <int N>
 __device__ __forceinline__ void rs_block_reduce(float* v, const int* op, float (*red)[RS_THREADS / 32]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -102,7 +103,6 @@ __device__ __forceinline__ void rs_block_reduce(float* v, const int* op, float (
       const float w = __shfl_xor_sync(0xffffffffu, v[k], o);
       v[k] = op[k] ? fmax_nan(v[k], w) : v[k] + w;
     }
-  __syncthreads();   // the previous use of red[] is finished
   if (lane == 0)
 #pragma unroll
     for (int k = 0; k < N; ++k) red[k][warp] = v[k];
@@ -131,7 +131,7 @@ template <class TP, class TQ, bool PROBS>
 __global__ void __launch_bounds__(RS_THREADS) row_stats_kernel(RowStatsArgs a) {
   extern __shared__ __align__(128) unsigned char rs_smem[];
   __shared__ __align__(8) uint64_t bar;
-  __shared__ float red[4][RS_THREADS / 32];
+  __shared__ float red[3][4][RS_THREADS / 32];   // one scratch array per pass
   __shared__ float xa[2][RS_MAX_CLUSTER];   // pass A: M_p, M_q
   __shared__ float xb[4][RS_MAX_CLUSTER];   // pass B: S_p, S_q, D (or bad q), timeout
   __shared__ float xc[3][RS_MAX_CLUSTER];   // pass C: alpha, (probs) tv, kl
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(RS_THREADS) row_stats_kernel(RowStatsArgs a) {
   }
   {
     const int op[2] = {1, 1};
-    rs_block_reduce<2>(mx, op, red);
+    rs_block_reduce<2>(mx, op, red[0]);
   }
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   rs_exchange<2>(mx, xa, rank, CS);
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(RS_THREADS) row_stats_kernel(RowStatsArgs a) {
   vb[3] = static_cast<float>(s_timeout);
   {
     const int op[4] = {0, PROBS ? 1 : 0, 0, 1};
-    rs_block_reduce<4>(vb, op, red);
+    rs_block_reduce<4>(vb, op, red[1]);
   }
   rs_exchange<4>(vb, xb, rank, CS);
   float Sp = 0.f, Sq = 0.f, Dq = 0.f, badq = 0.f, tmo = 0.f;
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(RS_THREADS) row_stats_kernel(RowStatsArgs a) {
   }
   {
     const int op[3] = {0, 0, 0};
-    rs_block_reduce<3>(vc, op, red);
+    rs_block_reduce<3>(vc, op, red[2]);
   }
   // only rank 0 needs the totals: publish to it alone (it is alive until the
   // barrier below completes, and no CTA touches a peer after that barrier)
