@@ -113,6 +113,14 @@ def test_sample_tiny_exactness(orc):
     P0 = sp_softmax(b.target[0, 0].astype(np.float64))
     _, pval = chisquare(np.bincount(out[:, 0], minlength=b.V), P0 * b.B)
     assert pval > 1e-3
+    # the pages' checks: empirical KL against the target below 0.01, and a small
+    # TV distance between speculative and plain target sampling
+    emp = np.bincount(out[:, 0], minlength=b.V) / b.B
+    direct = np.bincount(np.random.default_rng(13).choice(b.V, size=b.B, p=P0), minlength=b.V) / b.B
+    kl = float(np.sum(np.where(emp > 0, emp * np.log(np.where(emp > 0, emp, 1.0) / P0), 0.0)))
+    assert kl < 0.01
+    assert 0.5 * np.abs(emp - P0).sum() < 0.01
+    assert 0.5 * np.abs(emp - direct).sum() < 0.015
 
 
 @pytest.mark.parametrize("T", [1.0, 0.6])
