@@ -167,3 +167,18 @@ def test_tree_draft_rejects_bad_arguments(L):
     assert td(P(16), 9, P(32), 2, 8, 64, 4, F(1.0), P(48), P(64), None) == B.SPEC_ERR_INVALID_ARG
     assert td(P(16), B.SPEC_BF16, None, 2, 8, 64, 4, F(1.0), P(48), P(64), None) == B.SPEC_ERR_INVALID_ARG
     assert td(None, B.SPEC_BF16, None, 0, 8, 64, 4, F(1.0), None, None, None) == B.SPEC_OK
+
+
+def test_debug_stall_rejects_bad_arguments(L):
+    P, F = ctypes.c_void_p, ctypes.c_float
+    ds = L.spec_debug_stall
+
+    def call(stall_b=0, timeout_us=2000, T=0.7, Bn=4):
+        return ds(P(16), B.SPEC_BF16, P(32), B.SPEC_BF16, B.SPEC_DRAFT_LOGITS, P(48), P(64), F(T), Bn, 3, 64,
+                  stall_b, timeout_us, P(80), P(96), P(112), 1 << 20, None)
+
+    assert call(stall_b=-1) == B.SPEC_ERR_INVALID_ARG
+    assert call(stall_b=4) == B.SPEC_ERR_INVALID_ARG          # outside the batch
+    assert call(timeout_us=10) == B.SPEC_ERR_INVALID_ARG      # below 100 us
+    assert call(timeout_us=2_000_000) == B.SPEC_ERR_INVALID_ARG
+    assert call(T=0.0) == B.SPEC_ERR_INVALID_ARG              # the hook needs the sampling rule
