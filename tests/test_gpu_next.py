@@ -291,3 +291,23 @@ def test_draft_mask_verify_pipeline(orc):
     ro, rn, rp = orc.verify_tree_greedy(t, "bf16", par, tnp, int(depth.max()))
     np.testing.assert_array_equal(path.cpu().numpy(), rp)
     assert (rp[:, 0] == 2).all()
+
+
+def test_tree_draft_large_tree_multi_chunk(orc):
+    """A 700-node tree (the kernel scans the parent array in chunks of 256 to
+    find a node's children): random parents, at most 8 children per node."""
+    rng = np.random.default_rng(70)
+    N = 700
+    par = np.empty(N, np.int32)
+    par[0] = -1
+    kids = np.zeros(N, np.int64)
+    for i in range(1, N):
+        while True:
+            p = int(rng.integers(0, i))
+            if kids[p] < 8:
+                break
+        par[i] = p
+        kids[p] += 1
+    z = rng.standard_normal((3, N, 512)).astype(np.float32)
+    _draft_pair(orc, z, "f32", par, 0.9, 8)
+    _draft_pair(orc, gen._store(z.astype(np.float64), "bf16"), "bf16", par, 0.9, 8)
