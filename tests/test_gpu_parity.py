@@ -453,3 +453,30 @@ def test_non_default_stream(orc):
     s.synchronize()
     ref = gu.oracle_sample(orc, b)
     gu.compare_sample(out.cpu().numpy(), n.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("K,V,probs", [(31, 4096, False), (20, 1003, False), (31, 2048, True)])
+def test_sample_long_drafts(orc, K, V, probs):
+    """Long drafts (up to the K = 31 limit: 63 rows per sequence, two per lane
+    of the accept scan) with a near-perfect draft, so that deep positions and
+    the bonus draw are reached; logits (fused path, and the scalar path for an
+    odd V) and draft probabilities."""
+    rng = np.random.default_rng(K * 7 + V)
+    B, T = 12, 1.0
+    z = rng.standard_normal((B, K + 1, V))
+    y = z[:, :K] + 0.05 * rng.standard_normal((B, K, V))
+    tgt = gen.f32_to_bf16_bits(z)
+    if probs:
+        dft = sp_softmax(gen.as_f64(gen.f32_to_bf16_bits(y), "bf16") / T, axis=-1).astype(np.float32)
+        yq = np.log(np.maximum(dft.astype(np.float64), 1e-300))
+    else:
+        dft = gen.f32_to_bf16_bits(y)
+        yq = gen.as_f64(dft, "bf16") / T
+    g = -np.log(-np.log(rng.random((B, K, V))))
+    tok = np.argmax(yq + g, axis=-1).astype(np.int32)
+    uni = rng.random((B, K + 1, 2), dtype=np.float32)
+    batch = gen.ChainBatch(B, K, V, T, "bf16", tgt, dft, probs, tok, uni)
+    ref = gu.oracle_sample(orc, batch)
+    out, n = gu.gpu_sample(batch)
+    gu.compare_sample(out, n, ref)
+    assert ref["num_accepted"].max() >= K // 2     # deep positions were reached
