@@ -37,6 +37,14 @@
  *   - Vector path: rows whose byte length V * elem_size is a multiple of 16 (and
  *     16-byte aligned base pointers) are streamed with bulk async copies; other
  *     shapes take a scalar path with identical results.
+ *   - The vector-path kernels of spec_verify_sample, spec_verify_greedy and
+ *     spec_verify_tree_greedy are persistent grids whose CTAs wait on one
+ *     another (fixed owner CTAs per sequence, shared work queues), so they are
+ *     launched cooperatively: the grid is sized to what the device holds at
+ *     once, and where fewer SMs are available than the device reports (an MPS
+ *     share, a green context, another cooperative kernel running) the launch
+ *     fails with SPEC_ERR_CUDA instead of starting a grid that could stall.
+ *     The sampling kernel clears its own control block, so it needs no memset.
  *   - No C++ exception crosses this interface.
  */
 #ifndef SPEC_VERIFY_H
@@ -123,7 +131,9 @@ spec_status_t spec_verify_sample(const void *target_logits, spec_dtype_t target_
  * The first call on each device (with that device current) looks up the
  * array's device address with cudaGetSymbolAddress, which may load the
  * library's device code; make that first call before any stream capture.
- * Later calls on that device reuse the address.
+ * Later calls on that device reuse the address while its context lives: the
+ * first call after the context was re-created (cudaDeviceReset, or a released
+ * and re-created primary context) looks the address up again.
  *
  * The array is shared by every call on a device: calls that may overlap on the
  * GPU (different streams, different host threads) race on it and must be

@@ -33,10 +33,20 @@
 //              pick finds the 256-element block holding u*R from the block
 //              sums, re-reads that block, and locates the token with a
 //              warp-wide prefix scan.
-// Every wait (stage barriers, readiness and counter polling) is bounded in
-// time; a timeout sets an error word, and the last CTA to leave then marks
-// every sequence -2.
+// The fixed roles above (owner CTAs of scans and picks, residual units dealt
+// round-robin) need every CTA of the grid resident at once.  The kernel is
+// therefore launched cooperatively: a grid that cannot be resident fails at
+// launch instead of leaving resident CTAs waiting on CTAs that never start.
+// The kernel clears its own control block (each CTA a share) and meets at one
+// bounded grid barrier, so a call needs no memset; each producer's first
+// FU_STATIC_UNITS sweep units need no claim and stream while the barrier
+// completes.
+// Every wait (stage barriers, the grid barrier, readiness and counter polling)
+// is bounded in time; a timeout sets an error word, and the last CTA to leave
+// then marks every sequence -2.
 #pragma once
+
+#include <cooperative_groups.h>
 
 #include <type_traits>
 
@@ -61,6 +71,7 @@ constexpr int FU_BLK = 256;                       // residual block (elements)
 constexpr int FU_FLAG_STRIDE = 8;
 constexpr int FU_IDLE_NS = 256;                   // finisher's sleep between idle polls
 constexpr int FU_WSLOTS = 16;                     // sweep units whose warp partials await their merge
+constexpr int FU_STATIC_UNITS = 3;                // sweep units per CTA taken without a claim (blockIdx + k * grid)
 
 enum : int { KIND_STOP = -1, KIND_SWEEP = 0, KIND_RESID = 1 };
 enum : int { FL_FIRST = 1, FL_LAST = 2, FL_DRAFT = 4, FL_HASQ = 8 };
@@ -80,10 +91,10 @@ __device__ __forceinline__ unsigned fu_ready_word(int status, int tstar) {
   return 0x80000000u | (status != 0 ? 0x100u : 0u) | static_cast<unsigned>(tstar);
 }
 
-struct FuCtl {            // zeroed before every call (32 bytes reserved)
+struct FuCtl {            // cleared by the kernel before its grid barrier (32 bytes reserved)
   unsigned err;           // a wait timed out
   unsigned done;          // CTAs that have left
-  unsigned claim;         // sweep units claimed by the producers, in unit order
+  unsigned claim;         // sweep units claimed by the producers beyond the static ones, in unit order
 };
 static_assert(sizeof(FuCtl) <= 32, "control block must fit its 32-byte slot");
 
@@ -102,6 +113,7 @@ struct FusedArgs {
   int NB;                        // residual blocks per row = ceil(V / 256)
   unsigned U;                    // sweep units = B * RB * S
   float c;                       // log2(e) / T
+  unsigned zero_words;           // 16-byte words of [ctl | flags] the kernel clears
   FuCtl* ctl;
   unsigned* flags;               // [B * FU_FLAG_STRIDE]: per sequence, words 0 (sweep units completed),
                                  // 1 (residual units completed), 2 (1 once the accept scan wrote SeqInfo)
@@ -129,6 +141,7 @@ struct FuShared {
   unsigned res_word;             // readiness word of sequence res_have
   int res_want;                  // sequence of the producer's next residual unit (-1: none)
   int res_have;                  // sequence whose readiness word is in res_word (-1: none)
+  int grid_ready;                // the control block is cleared on every CTA (set by the merger warp)
   int abort;
 };
 
@@ -142,6 +155,38 @@ __device__ __forceinline__ bool fu_aborted(const FuShared& sh) {
 __device__ __forceinline__ void fu_fail(FuShared& sh, FuCtl* ctl, unsigned bit) {
   *reinterpret_cast<volatile int*>(&sh.abort) = 1;
   atomicOr(&ctl->err, bit);
+}
+
+// Wait (bounded) until the merger warp has seen the grid barrier pass, i.e.
+// every CTA has cleared its share of the control block.
+__device__ __forceinline__ bool fu_wait_grid(FuShared& sh, unsigned long long timeout_ns) {
+  if (*reinterpret_cast<volatile int*>(&sh.grid_ready) != 0) return true;
+  const uint64_t t0 = global_ns();
+  while (*reinterpret_cast<volatile int*>(&sh.grid_ready) == 0) {
+    if (fu_aborted(sh) || global_ns() - t0 > timeout_ns) return false;
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// One grid-wide barrier on the barrier word the driver provides to
+// cooperative launches (its flip-bit protocol: CTA 0 adds 2^31 - (G - 1), the
+// others 1, so bit 31 flips once all G have arrived).  Called by one thread
+// per CTA; gives up after timeout_ns and returns false.
+__device__ __forceinline__ bool fu_grid_barrier(unsigned long long timeout_ns) {
+  namespace cg = cooperative_groups;
+  cg::details::grid_workspace* ws = cg::details::get_grid_workspace();
+  if (ws == nullptr) return false;   // not a cooperative launch
+  unsigned* bar = &ws->barrier;
+  const unsigned nb = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1u) : 1u;
+  unsigned old;
+  asm volatile("atom.add.release.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(bar), "r"(nb) : "memory");
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (((old ^ ld_acquire_u32(bar)) & 0x80000000u) != 0u) return true;
+    if (global_ns() - t0 > timeout_ns) return false;
+    __nanosleep(128);
+  }
 }
 
 // element loaders for 8 consecutive elements (16 B of bf16, 32 B of f32)
@@ -826,12 +871,16 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
   // finisher warp has read (and then merges) the partials left in it.
   int unit_seq = 0;
 
-  // Sweep units are claimed from one counter, in unit order (sequence-major),
-  // one unit ahead so the claim's latency is hidden.  The loop acquires one
-  // ring stage at a time and then decides what fills it: the next residual
-  // unit if its sequence is ready, else the next stage of the current sweep
-  // unit.
-  unsigned next_claim = atomicAdd(&a.ctl->claim, 1u);
+  // Sweep units: this CTA's FU_STATIC_UNITS static units (blockIdx + k * grid)
+  // first, then units claimed from one counter in unit order (sequence-major),
+  // one claim ahead so its latency is hidden.  The first claim is issued once
+  // the grid barrier has passed (the counter is cleared by then).  The loop
+  // acquires one ring stage at a time and then decides what fills it: the
+  // next residual unit if its sequence is ready, else the next stage of the
+  // current sweep unit.
+  int static_taken = 0;
+  bool claiming = false, sweep_open = true;
+  unsigned next_claim = 0;
   bool ok = true;
   // current sweep unit and its partial slot
   bool have = false;
@@ -843,15 +892,37 @@ __device__ void fu_producer(const FusedArgs& a, unsigned char* ring, FuShared& s
   uint32_t bytes = 0, off = 0;
   while (ok) {
     if (!next_stage()) break;
+    if (!claiming && *reinterpret_cast<volatile int*>(&sh.grid_ready) != 0) {
+      next_claim = atomicAdd(&a.ctl->claim, 1u);
+      claiming = true;
+    }
     if (res_is_ready()) {
       ok = issue_resid();
       continue;
     }
     if (!have) {
       long long uid = -1;
-      if (next_claim < a.U) {
-        uid = next_claim;
-        next_claim = atomicAdd(&a.ctl->claim, 1u);
+      while (static_taken < FU_STATIC_UNITS && uid < 0) {
+        const long long cand = static_cast<long long>(blockIdx.x) + static_cast<long long>(static_taken) * G;
+        ++static_taken;
+        if (cand < static_cast<long long>(a.U)) uid = cand;
+      }
+      if (uid < 0 && sweep_open) {
+        if (!claiming) {
+          if (!fu_wait_grid(sh, a.timeout_ns)) {
+            if (!fu_aborted(sh)) fu_fail(sh, a.ctl, 256u);
+            break;
+          }
+          next_claim = atomicAdd(&a.ctl->claim, 1u);
+          claiming = true;
+        }
+        const long long cand = static_cast<long long>(FU_STATIC_UNITS) * G + next_claim;
+        if (cand < static_cast<long long>(a.U)) {
+          uid = cand;
+          next_claim = atomicAdd(&a.ctl->claim, 1u);
+        } else {
+          sweep_open = false;
+        }
       }
       if (uid < 0) {
         // no sweep work left: the remaining residual units, as their sequences become ready
@@ -1010,16 +1081,44 @@ __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& s
 // over, off the consumers' and the producer's paths
 // ---------------------------------------------------------------------------
 __device__ void fu_merger(const FusedArgs& a, FuShared& sh, int lane) {
+  // clear this CTA's share of the control block, then the grid barrier
+  {
+    uint4* z = reinterpret_cast<uint4*>(a.ctl);
+    for (unsigned i = blockIdx.x * 32u + static_cast<unsigned>(lane); i < a.zero_words; i += gridDim.x * 32u)
+      z[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    __threadfence();
+    // If the barrier gives up, a CTA that had not yet cleared its share could
+    // still clear the error word; the limit is 1 s, far beyond the microseconds
+    // co-resident CTAs take to arrive.
+    int passed = 1;
+    if (lane == 0) passed = fu_grid_barrier(a.timeout_ns) ? 1 : 0;
+    if (__shfl_sync(0xffffffffu, passed, 0) == 0) {
+      if (lane == 0) fu_fail(sh, a.ctl, 512u);
+    } else if (lane == 0) {
+      *reinterpret_cast<volatile int*>(&sh.grid_ready) = 1;
+    }
+  }
   const unsigned per_seq_units = static_cast<unsigned>(a.RB) * static_cast<unsigned>(a.S);
   int merged = 0;
   uint64_t last_progress = global_ns();
   for (;;) {
-    const int want = *reinterpret_cast<volatile int*>(&sh.res_want);
-    const int issued = *reinterpret_cast<volatile int*>(&sh.units_issued);
-    if (want < 0 && issued >= 0 && merged >= issued) break;
+    // Control decisions are taken on lane 0's reads and broadcast: a lane that
+    // read the shared words at another moment must not leave the loop (or skip
+    // a step) on its own, since the warp's shuffles below need every lane.
+    __syncwarp();
+    int want = -1, stop = 0, need_res = 0;
+    if (lane == 0) {
+      want = *reinterpret_cast<volatile int*>(&sh.res_want);
+      const int issued = *reinterpret_cast<volatile int*>(&sh.units_issued);
+      stop = (want < 0 && issued >= 0 && merged >= issued) || fu_aborted(sh);
+      need_res = want >= 0 && *reinterpret_cast<volatile int*>(&sh.res_have) != want;
+    }
+    if (__shfl_sync(0xffffffffu, stop, 0)) break;
+    want = __shfl_sync(0xffffffffu, want, 0);
+    need_res = __shfl_sync(0xffffffffu, need_res, 0);
     bool progress = false;
     // the readiness poll is issued first and read after the merges
-    const bool need_res = want >= 0 && *reinterpret_cast<volatile int*>(&sh.res_have) != want;
     unsigned v = 0;
     if (lane == 0 && need_res) v = ld_relaxed_u32(fu_ready(a, want));
     {
@@ -1059,8 +1158,7 @@ __device__ void fu_merger(const FusedArgs& a, FuShared& sh, int lane) {
       last_progress = global_ns();
       continue;
     }
-    const bool stop = __any_sync(0xffffffffu, fu_aborted(sh) || global_ns() - last_progress > 4 * a.timeout_ns);
-    if (stop) {
+    if (__any_sync(0xffffffffu, global_ns() - last_progress > 4 * a.timeout_ns)) {
       if (lane == 0) fu_fail(sh, a.ctl, 64u);
       break;
     }
@@ -1081,6 +1179,11 @@ __device__ void fu_finisher(const FusedArgs& a, FuShared& sh, int lane) {
   unsigned bp = (blockIdx.x + G - G / 2) % G;            // next pick
   ScanInputs in{};
   if (bs < static_cast<unsigned>(a.B)) in = scan_inputs<TP, TQ, PROBS>(a, static_cast<int>(bs), lane);
+  // the counters polled below are valid once every CTA has cleared its share
+  if (!fu_wait_grid(sh, a.timeout_ns)) {
+    if (lane == 0 && !fu_aborted(sh)) fu_fail(sh, a.ctl, 256u);
+    return;
+  }
   uint64_t last_progress = global_ns();
   while (bs < static_cast<unsigned>(a.B) || bp < static_cast<unsigned>(a.B)) {
     bool progress = false;
@@ -1121,7 +1224,7 @@ __device__ void fu_finisher(const FusedArgs& a, FuShared& sh, int lane) {
 }
 
 // ---------------------------------------------------------------------------
-// the kernel
+// the kernel (cooperative launch: every CTA resident)
 // ---------------------------------------------------------------------------
 constexpr size_t fu_smem_bytes() { return FU_NSTAGE * FU_STAGE + sizeof(FuShared) + 128; }
 
@@ -1139,6 +1242,7 @@ __global__ void __launch_bounds__(FU_THREADS, FU_CTAS_PER_SM) fused_sample_kerne
     }
     sh.abort = 0;
     sh.res_have = -1;
+    sh.grid_ready = 0;
     sh.units_issued = -1;
     for (int i = 0; i < FU_WSLOTS; ++i) sh.slot_unit[i] = 0;
     // the sequence of this CTA's first residual unit, set before any warp

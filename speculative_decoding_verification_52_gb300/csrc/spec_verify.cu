@@ -64,16 +64,48 @@ struct DevInfo {
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 
-// per-kernel one-time attribute setup, per device
+// Unique id of the calling thread's current CUDA context, plus one (0: no
+// context yet, or the driver entry points are unavailable).  A device reset or
+// a re-created primary context gets a new id, so per-device caches keyed on it
+// are set up again instead of reusing state of a context that is gone.
+unsigned long long current_ctx_id() {
+  using GetCurrent = int (*)(void**);
+  using GetId = int (*)(void*, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(fn);
+    cudaGetLastError();
+  });
+  if (!get_current || !get_id) return 0;
+  void* ctx = nullptr;
+  if (get_current(&ctx) != 0 || !ctx) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != 0) return 0;
+  return id + 1;
+}
+
+// per-kernel one-time attribute setup, per device and context (attributes do
+// not survive a device reset); without a context id it runs every time
 template <class F>
 bool once_per_device(int dev, F&& f) {
-  static bool done[kMaxDevices] = {};
+  static unsigned long long done[kMaxDevices] = {};   // context id the setup ran in
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   if (dev < 0 || dev >= kMaxDevices) return false;
-  if (!done[dev]) {
+  const unsigned long long id = current_ctx_id();
+  if (id == 0 || done[dev] != id) {
     if (!f()) return false;
-    done[dev] = true;
+    done[dev] = current_ctx_id();   // (the setup may have created the context)
   }
   return true;
 }
@@ -176,16 +208,19 @@ spec_status_t launch_sweep(const DevInfo& di, int dev, bool vec, const unsigned 
 }
 
 // ---------------------------------------------------------------------------
-// test hook of spec_debug_stall: while set (on the calling thread), the fused
-// sampling kernel runs with this wait limit and one sequence's accept scan
-// waits for a sweep unit that never comes
+// test hooks of the sampling path, passed down by the diagnostic entry points
+// (spec_debug_residual: force a stop and dump the residual row; spec_debug_stall:
+// one sequence's accept scan waits for a sweep unit that never comes, with a
+// short wait limit).  Production calls pass none.
 // ---------------------------------------------------------------------------
-struct StallHook {
-  int b = -1;
+struct SampleHooks {
+  int debug_b = -1, debug_t = -1;
+  float* debug_row = nullptr;
+  float* debug_mass = nullptr;
+  int stall_b = -1;
   unsigned long long timeout_ns = 0;
-  bool applied = false;
+  bool applied = false;   // set when the fused kernel took the hooks
 };
-thread_local StallHook g_stall;
 
 // ---------------------------------------------------------------------------
 // profiling events
@@ -311,7 +346,7 @@ int finish_max_cluster(int dev) {
 }
 
 // Workspace of the fused sampling kernel:
-//   [FuCtl | flags[B * FU_FLAG_STRIDE]]   zeroed per call
+//   [FuCtl | flags[B * FU_FLAG_STRIDE]]   cleared by the kernel
 //   [info[B] | bsum[B * ceil(V/256)] | part[rows * S] (float4)]
 struct FusedLayout {
   size_t zero_bytes, info_off, bsum_off, part_off, total;
@@ -348,11 +383,11 @@ int fused_per_sm(int dev) {
 template <class TP, class TQ, bool PROBS>
 spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, const void* draft,
                                const int32_t* tokens, const float* uni, float c, int B, int K, int V, int32_t* out,
-                               int32_t* nacc, void* ws, int debug_b, int debug_t, float* debug_row,
-                               float* debug_mass, cudaStream_t st) {
+                               int32_t* nacc, void* ws, SampleHooks* hooks, cudaStream_t st) {
   constexpr int QE = PROBS ? 4 : TQ::esz;
   const int per_sm = fused_per_sm<TP, TQ, PROBS>(dev);
   if (per_sm <= 0) return fail(SPEC_ERR_CUDA, "fused kernel setup failed: %s", cudaGetErrorString(cudaGetLastError()));
+  // a cooperative launch: the grid never exceeds what is resident at once
   const int grid_cap = std::min(FU_MAX_GRID, di.sms * per_sm);
   const int RB = PROBS ? K + 1 : 2 * K + 1;
   const long long rows = static_cast<long long>(B) * RB;
@@ -370,12 +405,12 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
     L = (ceil_div(V, smax) + 7) / 8 * 8;
     S = ceil_div(V, L);
   }
-  int grid = grid_cap;
   const long long U = rows * S;
-  if (U >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "batch too large for one call");
   const int RE = (TP::esz == 2 && QE == 2) ? 4096 : 2048;   // residual stage: 16 KB of P+Q at most
   const int Lr = 2 * RE;
   const int Sr = ceil_div(V, Lr);
+  const long long RU = static_cast<long long>(B) * Sr;
+  if (U >= (1LL << 31) || RU >= (1LL << 31)) return fail(SPEC_ERR_UNSUPPORTED, "batch too large for one call");
 
   const FusedLayout lay = fused_layout(B, K, V);
   unsigned char* w = static_cast<unsigned char*>(ws);
@@ -398,30 +433,38 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
   a.NB = ceil_div(V, FU_BLK);
   a.ctl = reinterpret_cast<FuCtl*>(w);
   a.flags = reinterpret_cast<unsigned*>(w + 32);
+  a.zero_words = static_cast<unsigned>(lay.zero_bytes / 16);
   a.info = reinterpret_cast<SeqInfo*>(w + lay.info_off);
   a.bsum = reinterpret_cast<float*>(w + lay.bsum_off);
   a.part = reinterpret_cast<float4*>(w + lay.part_off);
   a.out_tokens = out;
   a.num_accepted = nacc;
-  a.debug_b = debug_b;
-  a.debug_t = debug_t;
-  a.debug_row = debug_row;
-  a.debug_mass = debug_mass;
+  a.debug_b = hooks ? hooks->debug_b : -1;
+  a.debug_t = hooks ? hooks->debug_t : -1;
+  a.debug_row = hooks ? hooks->debug_row : nullptr;
+  a.debug_mass = hooks ? hooks->debug_mass : nullptr;
   a.timeout_ns = kWaitNs;
   a.debug_stall_b = -1;
-  if (g_stall.b >= 0) {   // test hook (spec_debug_stall)
-    a.debug_stall_b = g_stall.b;
-    a.timeout_ns = g_stall.timeout_ns;
-    g_stall.applied = true;
+  if (hooks && hooks->stall_b >= 0) {   // test hook (spec_debug_stall)
+    a.debug_stall_b = hooks->stall_b;
+    a.timeout_ns = hooks->timeout_ns;
+    hooks->applied = true;
   }
-  cudaError_t e = cudaMemsetAsync(ws, 0, lay.zero_bytes, st);
-  if (e != cudaSuccess) return cuda_fail(e, "workspace control reset");
+  const long long work = U + RU;
+  const int grid = static_cast<int>(std::min<long long>(grid_cap, work));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(FU_THREADS);
+  cfg.dynamicSmemBytes = fu_smem_bytes();
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_mark(0, st);
-  const long long work = U + static_cast<long long>(B) * Sr;
-  grid = static_cast<int>(std::min<long long>(grid, work));
-  fused_sample_kernel<TP, TQ, PROBS><<<grid, FU_THREADS, fu_smem_bytes(), st>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "fused sampling launch");
+  cudaError_t e = cudaLaunchKernelEx(&cfg, fused_sample_kernel<TP, TQ, PROBS>, a);
+  if (e != cudaSuccess) return cuda_fail(e, "fused sampling launch (cooperative)");
   prof_mark(1, st);
   prof_mark(2, st);
   return SPEC_OK;
@@ -430,14 +473,14 @@ spec_status_t run_sample_fused(const DevInfo& di, int dev, const void* target, c
 template <class TP, class TQ, bool PROBS>
 spec_status_t run_sample(const DevInfo& di, int dev, const void* target, const void* draft, const int32_t* tokens,
                          const float* uni, float T, int B, int K, int V, int32_t* out, int32_t* nacc, void* ws,
-                         int debug_b, int debug_t, float* debug_row, float* debug_mass, cudaStream_t st) {
+                         SampleHooks* hooks, cudaStream_t st) {
   constexpr int QE = PROBS ? 4 : TQ::esz;
   const bool vec = aligned16(target) && (static_cast<long long>(V) * TP::esz) % 16 == 0 &&
                    (K == 0 || (aligned16(draft) && (static_cast<long long>(V) * QE) % 16 == 0)) && V % 8 == 0;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
   if (vec)
-    return run_sample_fused<TP, TQ, PROBS>(di, dev, target, draft, tokens, uni, c, B, K, V, out, nacc, ws, debug_b,
-                                           debug_t, debug_row, debug_mass, st);
+    return run_sample_fused<TP, TQ, PROBS>(di, dev, target, draft, tokens, uni, c, B, K, V, out, nacc, ws, hooks,
+                                           st);
 
   // scalar path for unaligned rows: sweep kernel + clustered finishing kernel
   const long long rows0 = static_cast<long long>(B) * (K + 1);
@@ -463,10 +506,10 @@ spec_status_t run_sample(const DevInfo& di, int dev, const void* target, const v
   a.c = c;
   a.out_tokens = out;
   a.num_accepted = nacc;
-  a.debug_b = debug_b;
-  a.debug_t = debug_t;
-  a.debug_row = debug_row;
-  a.debug_mass = debug_mass;
+  a.debug_b = hooks ? hooks->debug_b : -1;
+  a.debug_t = hooks ? hooks->debug_t : -1;
+  a.debug_row = hooks ? hooks->debug_row : nullptr;
+  a.debug_mass = hooks ? hooks->debug_mass : nullptr;
 
   const int maxcl = finish_max_cluster<TP, TQ, PROBS, false>(dev);
   int CL = std::min(maxcl, std::max(1, ceil_div(V, 8192)));
@@ -485,10 +528,9 @@ spec_status_t run_sample(const DevInfo& di, int dev, const void* target, const v
 
 spec_status_t dispatch_sample(const DevInfo& di, int dev, const void* target, spec_dtype_t tdt, const void* draft,
                               spec_dtype_t ddt, spec_draft_kind_t kind, const int32_t* tokens, const float* uni,
-                              float T, int B, int K, int V, int32_t* out, int32_t* nacc, void* ws, int debug_b,
-                              int debug_t, float* drow, float* dmass, cudaStream_t st) {
-#define SV_RUN(TP, TQ, PR) \
-  run_sample<TP, TQ, PR>(di, dev, target, draft, tokens, uni, T, B, K, V, out, nacc, ws, debug_b, debug_t, drow, dmass, st)
+                              float T, int B, int K, int V, int32_t* out, int32_t* nacc, void* ws,
+                              SampleHooks* hooks, cudaStream_t st) {
+#define SV_RUN(TP, TQ, PR) run_sample<TP, TQ, PR>(di, dev, target, draft, tokens, uni, T, B, K, V, out, nacc, ws, hooks, st)
   const bool probs = kind == SPEC_DRAFT_PROBS;
   if (tdt == SPEC_BF16) {
     if (probs) return SV_RUN(BF16T, F32T, true);
@@ -582,9 +624,21 @@ spec_status_t run_tree_pruned(const DevInfo& di, int dev, const void* target, co
   cudaError_t e = cudaMemsetAsync(ws, 0, lay.zero_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "tree workspace reset");
   prof_mark(0, st);
-  tree_greedy_kernel<T><<<grid, TR_THREADS, tr_smem_bytes(), st>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "tree kernel launch");
+  // a cooperative launch: the finisher of CTA b mod grid owns sequence b and
+  // producers wait on FIFO slots other CTAs fill, so every CTA must be
+  // resident; a grid that cannot be fails here instead of stalling
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(TR_THREADS);
+  cfg.dynamicSmemBytes = tr_smem_bytes();
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, tree_greedy_kernel<T>, a);
+  if (e != cudaSuccess) return cuda_fail(e, "tree kernel launch (cooperative)");
   prof_mark(1, st);
   prof_mark(2, st);
   return SPEC_OK;
@@ -614,8 +668,8 @@ spec_status_t check_ws(void* ws, size_t have, size_t need) {
 
 spec_status_t sample_entry(const void* target, spec_dtype_t tdt, const void* draft, spec_dtype_t ddt,
                            spec_draft_kind_t kind, const int32_t* tokens, const float* uni, float T, int B, int K,
-                           int V, int32_t* out, int32_t* nacc, void* ws, size_t wsb, int debug_b, int debug_t,
-                           float* drow, float* dmass, void* stream) {
+                           int V, int32_t* out, int32_t* nacc, void* ws, size_t wsb, SampleHooks* hooks,
+                           void* stream) {
   spec_status_t s = check_chain_args(target, tdt, tokens, B, K, V, out, nacc);
   if (s != SPEC_OK || B == 0) return s;
   if (!(T >= 0.f) || !std::isfinite(T)) return fail(SPEC_ERR_INVALID_ARG, "temperature %g must be finite and >= 0", T);
@@ -637,7 +691,7 @@ spec_status_t sample_entry(const void* target, spec_dtype_t tdt, const void* dra
   }
   if (V > FS_MAX_L * 16) return fail(SPEC_ERR_UNSUPPORTED, "V=%d above the sampling limit %d", V, FS_MAX_L * 16);
   return dispatch_sample(di, dev, target, tdt, draft, K > 0 ? ddt : SPEC_F32, kind, tokens, uni, T, B, K, V, out,
-                         nacc, ws, debug_b, debug_t, drow, dmass, st);
+                         nacc, ws, hooks, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -713,19 +767,25 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 namespace {
 
 // Device address of the array in the current device's context.  Resolved once
-// per device, on the first call made with that device current; later calls
-// only read the cached pointer.
+// per device and context, on the first call made with that device current;
+// later calls in the same context only read the cached pointer.  A call in a
+// new context of the device (after cudaDeviceReset, or once the primary
+// context was released and re-created) resolves it again, since the array then
+// lives at a new address.
 spec_status_t noalloc_scratch(int dev, void** out) {
   static void* ptr[kMaxDevices] = {};
+  static unsigned long long ctx[kMaxDevices] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   if (dev < 0 || dev >= kMaxDevices) return fail(SPEC_ERR_UNSUPPORTED, "device ordinal %d", dev);
-  if (!ptr[dev]) {
+  const unsigned long long id = current_ctx_id();
+  if (!ptr[dev] || id == 0 || ctx[dev] != id) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed scratch)");
     if (!p) return fail(SPEC_ERR_CUDA, "cudaGetSymbolAddress returned a NULL scratch address");
     ptr[dev] = p;
+    ctx[dev] = current_ctx_id();   // (the lookup may have created the context)
   }
   *out = ptr[dev];
   return SPEC_OK;
@@ -759,8 +819,7 @@ spec_status_t spec_verify_sample(const void* target_logits, spec_dtype_t target_
                                  int32_t* num_accepted, void* workspace, size_t workspace_bytes, void* stream) {
   try {
     return sample_entry(target_logits, target_dtype, draft, draft_dtype, draft_kind, draft_tokens, uniforms,
-                        temperature, B, K, V, out_tokens, num_accepted, workspace, workspace_bytes, -1, -1, nullptr,
-                        nullptr, stream);
+                        temperature, B, K, V, out_tokens, num_accepted, workspace, workspace_bytes, nullptr, stream);
   } catch (...) {
     return fail(SPEC_ERR_CUDA, "unexpected host exception");
   }
@@ -774,8 +833,7 @@ spec_status_t spec_verify_sample_noalloc(const void* target_logits, spec_dtype_t
     const size_t need = spec_workspace_bytes(B, K, V);
     if (B == 0 || need == 0)   // empty batch or bad sizes: argument checks only, nothing launched
       return sample_entry(target_logits, target_dtype, draft, draft_dtype, draft_kind, draft_tokens, uniforms,
-                          temperature, B, K, V, out_tokens, num_accepted, nullptr, 0, -1, -1, nullptr, nullptr,
-                          stream);
+                          temperature, B, K, V, out_tokens, num_accepted, nullptr, 0, nullptr, stream);
     if (need > kNoallocScratchBytes)
       return fail(SPEC_ERR_UNSUPPORTED,
                   "B=%d K=%d V=%d needs %zu scratch bytes; spec_verify_sample_noalloc holds %zu "
@@ -788,8 +846,7 @@ spec_status_t spec_verify_sample_noalloc(const void* target_logits, spec_dtype_t
     spec_status_t s = noalloc_scratch(dev, &ws);
     if (s != SPEC_OK) return s;
     return sample_entry(target_logits, target_dtype, draft, draft_dtype, draft_kind, draft_tokens, uniforms,
-                        temperature, B, K, V, out_tokens, num_accepted, ws, kNoallocScratchBytes, -1, -1, nullptr,
-                        nullptr, stream);
+                        temperature, B, K, V, out_tokens, num_accepted, ws, kNoallocScratchBytes, nullptr, stream);
   } catch (...) {
     return fail(SPEC_ERR_CUDA, "unexpected host exception");
   }
@@ -805,9 +862,13 @@ spec_status_t spec_debug_residual(const void* target_logits, spec_dtype_t target
       return fail(SPEC_ERR_INVALID_ARG, "debug position (%d, %d) outside the batch", debug_b, debug_t);
     if (!out_row || !out_mass) return fail(SPEC_ERR_INVALID_ARG, "NULL out_row/out_mass");
     if (!(temperature > 0.f)) return fail(SPEC_ERR_INVALID_ARG, "the residual needs temperature > 0");
+    SampleHooks hooks;
+    hooks.debug_b = debug_b;
+    hooks.debug_t = debug_t;
+    hooks.debug_row = out_row;
+    hooks.debug_mass = out_mass;
     return sample_entry(target_logits, target_dtype, draft, draft_dtype, draft_kind, draft_tokens, uniforms,
-                        temperature, B, K, V, out_tokens, num_accepted, workspace, workspace_bytes, debug_b, debug_t,
-                        out_row, out_mass, stream);
+                        temperature, B, K, V, out_tokens, num_accepted, workspace, workspace_bytes, &hooks, stream);
   } catch (...) {
     return fail(SPEC_ERR_CUDA, "unexpected host exception");
   }
@@ -1112,16 +1173,13 @@ spec_status_t spec_debug_stall(const void* target_logits, spec_dtype_t target_dt
     if (timeout_us < 100 || timeout_us > 1000000u)
       return fail(SPEC_ERR_INVALID_ARG, "timeout_us=%u outside [100, 1000000]", timeout_us);
     if (!(temperature > 0.f)) return fail(SPEC_ERR_INVALID_ARG, "the stall hook needs the sampling rule (T > 0)");
-    struct Reset {
-      ~Reset() { g_stall = StallHook{}; }
-    } reset;
-    g_stall.b = stall_b;
-    g_stall.timeout_ns = static_cast<unsigned long long>(timeout_us) * 1000ull;
-    g_stall.applied = false;
+    SampleHooks hooks;
+    hooks.stall_b = stall_b;
+    hooks.timeout_ns = static_cast<unsigned long long>(timeout_us) * 1000ull;
     spec_status_t s = sample_entry(target_logits, target_dtype, draft, draft_dtype, draft_kind, draft_tokens,
                                    uniforms, temperature, B, K, V, out_tokens, num_accepted, workspace,
-                                   workspace_bytes, -1, -1, nullptr, nullptr, stream);
-    if (s == SPEC_OK && !g_stall.applied)
+                                   workspace_bytes, &hooks, stream);
+    if (s == SPEC_OK && !hooks.applied)
       return fail(SPEC_ERR_UNSUPPORTED, "the stall hook needs the fused sampling path (16-byte aligned rows)");
     return s;
   } catch (...) {

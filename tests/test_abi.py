@@ -25,9 +25,9 @@ def test_exports_every_declared_symbol(L):
 
 def test_workspace_sizes(L):
     # control block (32 B) + per-sequence counters and readiness flags (one
-    # 32-byte block each), per-sequence info (32 B), residual
-    # block sums (ceil(V/256) floats per sequence), and one 16-byte partial per
-    # sweep unit (rows x at most ceil(V/2048) slices)
+    # 32-byte block each), per-sequence info (32 B), residual block sums
+    # (ceil(V/256) floats per sequence), and one 16-byte partial per sweep
+    # unit (rows x at most ceil(V/2048) slices)
     def al(x, a):
         return (x + a - 1) // a * a
     B_, K_, V_ = 256, 5, 128256

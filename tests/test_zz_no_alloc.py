@@ -65,3 +65,66 @@ def test_noalloc_matches_workspace_entry_point_twice(orc, cfg):
         compare_sample(o, n, oracle_sample(orc, batch))
         out.fill_(-7)
         nacc.fill_(-7)
+
+
+@pytest.mark.gpu
+def test_noalloc_greedy_twice_matches_greedy_entry_point(orc):
+    """T = 0 sends the fixed scratch through the greedy chain kernel, whose
+    layout differs from the sampling kernel's: two calls in a row must match
+    spec_verify_greedy and the oracle bit for bit."""
+    import torch
+
+    import speculative_decoding_verification_52_gb300 as sv
+    from gpu_util import DEV, dev_tensor, i32
+
+    batch = gen.config_greedy(seqs=list(range(96)))
+    Bn, K = batch.B, batch.K
+    target = dev_tensor(batch.target, batch.dtype)
+    tok = i32(batch.draft_tokens)
+    ro, rn = orc.verify_greedy(batch.target, batch.dtype, batch.draft_tokens)
+    go, gn = sv.spec_verify_greedy(target, tok)
+    np.testing.assert_array_equal(gn.cpu().numpy(), rn)
+    np.testing.assert_array_equal(go.cpu().numpy(), ro)
+    # the sampling signature at T = 0: draft and uniforms are not read
+    out = torch.full((Bn, K + 1), -7, dtype=torch.int32, device=DEV)
+    nacc = torch.full((Bn,), -7, dtype=torch.int32, device=DEV)
+    for call in range(2):
+        sv.spec_verify_sample_noalloc(target, None, tok, None, 0.0, out_tokens=out, num_accepted=nacc)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(nacc.cpu().numpy(), rn, err_msg=f"call {call}: num_accepted differs")
+        np.testing.assert_array_equal(out.cpu().numpy(), ro, err_msg=f"call {call}: out_tokens differ")
+        out.fill_(-7)
+        nacc.fill_(-7)
+
+
+@pytest.mark.gpu
+def test_noalloc_sampling_then_greedy_then_sampling(orc):
+    """Calls of the two kernels share the fixed scratch in turn: what one
+    leaves in it (control words, counters, queue slots) must not leak into
+    the next call of the other."""
+    import torch
+
+    import speculative_decoding_verification_52_gb300 as sv
+    from gpu_util import DEV, compare_sample, dev_tensor, f32, i32, oracle_sample
+
+    sb = gen.config_headline(seqs=list(range(48)))
+    gb = gen.config_greedy(seqs=list(range(48)))
+    st, sd = dev_tensor(sb.target, sb.dtype), dev_tensor(sb.draft, sb.draft_dtype)
+    stok, suni = i32(sb.draft_tokens), f32(sb.uniforms)
+    gt, gtok = dev_tensor(gb.target, gb.dtype), i32(gb.draft_tokens)
+    sref = oracle_sample(orc, sb)
+    ro, rn = orc.verify_greedy(gb.target, gb.dtype, gb.draft_tokens)
+    out = torch.empty((sb.B, sb.K + 1), dtype=torch.int32, device=DEV)
+    nacc = torch.empty((sb.B,), dtype=torch.int32, device=DEV)
+    for step in ("sample", "greedy", "sample", "greedy"):
+        out.fill_(-7)
+        nacc.fill_(-7)
+        if step == "sample":
+            sv.spec_verify_sample_noalloc(st, sd, stok, suni, sb.T, out_tokens=out, num_accepted=nacc)
+            torch.cuda.synchronize()
+            compare_sample(out.cpu().numpy(), nacc.cpu().numpy(), sref)
+        else:
+            sv.spec_verify_sample_noalloc(gt, None, gtok, None, 0.0, out_tokens=out, num_accepted=nacc)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(nacc.cpu().numpy(), rn)
+            np.testing.assert_array_equal(out.cpu().numpy(), ro)
