@@ -8,6 +8,14 @@ per-sequence accept scan and replacement/bonus draw, all inside one persistent
 kernel launch (after a small memset of the workspace's control block).
 
 Other workloads (--workload):
+  zipf    spec_verify_sample, B=64, V=32000, K=4, f32, T=1: target 2*N(0,1) with
+          a Zipf-like bias -1.1*log(rank) over a random vocabulary permutation,
+          draft = target + N(0, 0.7^2)
+  zipf_greedy  spec_verify_greedy on the same inputs (the temperature-0 run)
+  ctl_B<B>_K<K>  spec_verify_sample over the controlled-acceptance sweep,
+          V=151936 bf16 T=1, B in {1, 8, 64, 512}, K in {4, 8}: each draft row is
+          a copy of its target row with probability 0.8, else an independent row
+  sweep   all eight ctl_B<B>_K<K> workloads in one run, one JSON line each
   greedy  spec_verify_greedy, B=256, V=128256, K=5, bf16; draft token t is the
           target row's argmax with probability 0.8
   tree    spec_verify_tree_greedy, B=128, N=64 nodes (BFS [4,3,2,1] truncated),
@@ -24,8 +32,10 @@ Inputs are generated once (seeded, synthetic), copied to HBM, and the timed
 region covers exactly --steps calls bracketed by a barrier and a device
 synchronisation, timed with CUDA events; a second pass of --steps calls with
 the library's per-kernel event hooks gives the kernel durations the roofline
-uses.  Every workload's inputs are larger
-than the L2 cache (129 MB), so no flush is needed between steps.
+uses.  Inputs smaller than twice the L2 cache (129 MB) are held in several
+device copies that the steps cycle through, so every step reads inputs that
+at least one L2's worth of other traffic has passed since their last use; no
+flush is needed between steps.
 
 Reported: the metric (verified draft positions/s; tree: candidate nodes/s),
 the dominant kernel's achieved HBM bandwidth against the measured copy peak
@@ -33,8 +43,15 @@ the dominant kernel's achieved HBM bandwidth against the measured copy peak
 region, the SM clocks seen during the run, and the double-precision CPU
 oracle timed on a bounded sample on this host.
 
+The CPU baseline is the double-precision oracle on this host's cores (one
+thread per core, sequences split between threads; the single-threaded rate
+is reported beside it).  It runs on the first sequences of the timed batch,
+and the GPU outputs of those sequences are compared with the oracle's there
+(the parity block: bit-exact outside decisions the oracle flags as within
+1e-6 of flipping, flags counted).
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload sample|greedy|tree|treemask|kvcommit|stats|draft]
+                    [--workload sample|zipf|zipf_greedy|ctl_B<B>_K<K>|sweep|greedy|tree|treemask|kvcommit|stats|draft]
 """
 from __future__ import annotations
 
@@ -62,6 +79,15 @@ UNIT = "positions/s"
 def sweep_bytes(b=B, k=K, v=V, elem=2):
     """Bytes of one pass over every target and draft row."""
     return b * (2 * k + 1) * v * elem
+
+
+L2_BYTES = 129 * 10**6
+
+
+def rotation_copies(nbytes: int) -> int:
+    """Device copies of a step's inputs to cycle through so that copies x
+    bytes spans at least twice the L2 cache."""
+    return max(1, -(-2 * L2_BYTES // max(1, nbytes)))
 
 
 def metric_bytes(b=B, k=K, v=V, elem=2):
@@ -226,6 +252,11 @@ class Workload:
     def oracle_chunk(self) -> int:
         return 4
 
+    def parity(self, batch, outs, n):
+        """GPU outputs of the first n sequences against the oracle (None when
+        the workload has no parity summary here)."""
+        return None
+
     def device_setup(self, batch, dev):
         """Returns (host inputs, device inputs they are copied to, step(),
         device outputs)."""
@@ -242,6 +273,190 @@ def _pinned(x):
     import numpy as np
     import torch
     return torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+
+
+def sample_parity(batch, out, nacc, n):
+    """Sampling outputs of the first n sequences against the oracle: bit-exact
+    except after decisions the oracle flags as within 1e-6 of flipping (a near
+    accept test at t excludes slots >= t and the count; a near CDF boundary
+    excludes only the drawn token).  Counts flags and mismatches."""
+    import numpy as np
+
+    import oracle
+    sl = slice(0, n)
+    ref = oracle.verify_sample(batch.target[sl], batch.dtype, batch.draft[sl], batch.draft_dtype,
+                               batch.draft_is_probs, np.ascontiguousarray(batch.draft_tokens[sl]),
+                               np.ascontiguousarray(batch.uniforms[sl]), batch.T)
+    na, nc, ro, rn = ref["near_accept"], ref["near_cdf"], ref["out_tokens"], ref["num_accepted"]
+    flagged = flagged_mismatch = unflagged_mismatch = 0
+    for b in range(n):
+        if na[b] >= 0:
+            flagged += 1
+            t = int(na[b])
+            ok = bool((out[b, :t] == ro[b, :t]).all())
+            if not ok:
+                unflagged_mismatch += 1
+            elif nacc[b] != rn[b] or not (out[b] == ro[b]).all():
+                flagged_mismatch += 1
+            continue
+        if nacc[b] != rn[b]:
+            unflagged_mismatch += 1
+            continue
+        if nc[b]:
+            flagged += 1
+            tsl = int(rn[b]) if rn[b] >= 0 else 0
+            keep = np.ones(out.shape[1], dtype=bool)
+            keep[tsl] = False
+            if not (out[b][keep] == ro[b][keep]).all():
+                unflagged_mismatch += 1
+            elif out[b, tsl] != ro[b, tsl]:
+                flagged_mismatch += 1
+            continue
+        if not (out[b] == ro[b]).all():
+            unflagged_mismatch += 1
+    return {"sequences": n, "near_accept": int((na >= 0).sum()), "near_cdf": int((nc != 0).sum()),
+            "flagged_sequences": flagged, "flagged_mismatch": flagged_mismatch,
+            "unflagged_mismatch": unflagged_mismatch,
+            "rule": "bit-exact except after a decision within 1e-6 of flipping (counted)"}
+
+
+def greedy_parity(batch, out, nacc, n):
+    """Greedy outputs of the first n sequences against the oracle, bit for bit."""
+    import numpy as np
+
+    import oracle
+    ro, rn = oracle.verify_greedy(batch.target[:n], batch.dtype, np.ascontiguousarray(batch.draft_tokens[:n]))
+    bad = int(((nacc[:n] != rn) | (out[:n] != ro).any(axis=1)).sum())
+    return {"sequences": n, "mismatch": bad, "rule": "bit-exact"}
+
+
+class ChainWorkload(Workload):
+    """One chain-verification call (sampling, or the greedy rule) over a
+    ChainBatch, with the batch's inputs held in rotation_copies(...) device
+    copies that consecutive steps cycle through."""
+
+    def __init__(self, name, label, make, B_, K_, V_, T_, elem, greedy=False, summary="", kernel=""):
+        self.name, self.label, self.make = name, label, make
+        self.Bn, self.Kn, self.Vn, self.Tn, self.elem, self.greedy = B_, K_, V_, T_, elem, greedy
+        self.per_rank = B_
+        self.summary = summary
+        self.kernel = kernel or ("tree_greedy_kernel (chain mode)" if greedy else "fused_sample_kernel")
+        self.sources = ("common.cuh", "tree.cuh") if greedy else ("common.cuh", "fused.cuh")
+
+    def input_bytes(self):
+        if self.greedy:
+            return self.Bn * (self.Kn + 1) * self.Vn * self.elem
+        return self.Bn * (2 * self.Kn + 1) * self.Vn * self.elem
+
+    def describe(self):
+        nb = self.input_bytes()
+        c = rotation_copies(nb)
+        return {"workload": self.label, "B": self.Bn, "V": self.Vn, "K": self.Kn,
+                "temperature": 0.0 if self.greedy else self.Tn, "input_bytes": nb, "input_copies": c,
+                "l2": (f"inputs ({nb / 1e6:.1f} MB) larger than twice L2; no flush" if c == 1 else
+                       f"{c} device copies of the inputs ({c * nb / 1e6:.1f} MB) cycled: each step reads "
+                       f"inputs untouched for at least one L2's worth of traffic; no flush")}
+
+    def batch(self, seqs):
+        return self.make(seqs)
+
+    def units(self, batch):
+        return batch.B * batch.K
+
+    def algorithmic_bytes(self, batch):
+        if not self.greedy:
+            return metric_bytes(batch.B, batch.K, batch.V, self.elem)
+        # the greedy rule reads rows 0..n of a sequence that accepts n drafts
+        # (the argmax of the f32 target rows, first index on ties)
+        import numpy as np
+        g = np.argmax(batch.target, axis=-1)[:, :batch.K]
+        rows = int((leading_true(g == batch.draft_tokens) + 1).sum())
+        return rows * batch.V * self.elem
+
+    def oracle_call(self, batch, sl):
+        import numpy as np
+
+        import oracle
+        tok = np.ascontiguousarray(batch.draft_tokens[sl])
+        if self.greedy:
+            oracle.verify_greedy(batch.target[sl], batch.dtype, tok)
+        else:
+            oracle.verify_sample(batch.target[sl], batch.dtype, batch.draft[sl], batch.draft_dtype,
+                                 batch.draft_is_probs, tok, np.ascontiguousarray(batch.uniforms[sl]), batch.T)
+
+    def oracle_chunk(self):
+        return 1
+
+    def parity(self, batch, outs, n):
+        out, nacc = outs[0], outs[1]
+        return greedy_parity(batch, out, nacc, n) if self.greedy else sample_parity(batch, out, nacc, n)
+
+    def device_setup(self, batch, dev):
+        import torch
+
+        import speculative_decoding_verification_52_gb300 as sv
+        conv = _bf16_host if batch.dtype == "bf16" else _pinned
+        hs = [conv(batch.target)]
+        if not self.greedy:
+            hs.append(conv(batch.draft))
+        hs += [_pinned(batch.draft_tokens), _pinned(batch.uniforms)]
+        copies = rotation_copies(self.input_bytes())
+        sets = [[h.to(dev) for h in hs] for _ in range(copies)]
+        out = torch.empty((batch.B, batch.K + 1), dtype=torch.int32, device=dev)
+        nacc = torch.empty((batch.B,), dtype=torch.int32, device=dev)
+        wsb = sv.workspace(sv.spec_workspace_bytes(batch.B, batch.K, batch.V), dev)
+        stream = torch.cuda.current_stream()
+        i = [0]
+
+        def step():
+            d = sets[i[0]]
+            i[0] = (i[0] + 1) % copies
+            if self.greedy:
+                sv.spec_verify_greedy(d[0], d[1], out_tokens=out, num_accepted=nacc, workspace_buf=wsb,
+                                      stream=stream)
+            else:
+                sv.spec_verify_sample(d[0], d[1], d[2], d[3], batch.T, out_tokens=out, num_accepted=nacc,
+                                      workspace_buf=wsb, stream=stream)
+        # end to end: the host inputs are copied into the set the next step reads
+        return hs, _RotatingSets(sets, i), step, [out, nacc]
+
+
+class _RotatingSets:
+    """The device input set the next step reads (for the end-to-end copies)."""
+
+    def __init__(self, sets, index):
+        self.sets, self.index = sets, index
+
+    def __iter__(self):
+        return iter(self.sets[self.index[0]])
+
+
+def _zipf(T_):
+    def make(seqs):
+        from speculative_decoding_verification_52_gb300 import inputs as gen
+        return gen.config_zipf(T=T_, B=64, seqs=seqs)
+    return make
+
+
+def _controlled(B_, K_):
+    def make(seqs):
+        from speculative_decoding_verification_52_gb300 import inputs as gen
+        return gen.config_controlled(B_, K_, seqs=seqs)
+    return make
+
+
+SWEEP = [(b, k) for k in (4, 8) for b in (1, 8, 64, 512)]
+CHAIN_WORKLOADS = [
+    ChainWorkload("zipf", "spec-verify sampling B=64 V=32000 K=4 f32 T=1, Zipf-biased targets "
+                  "(2*N(0,1) - 1.1*log(rank)), draft = target + N(0,0.7^2)", _zipf(1.0), 64, 4, 32000, 1.0, 4),
+    ChainWorkload("zipf_greedy", "spec-verify greedy B=64 V=32000 K=4 f32, the Zipf-biased inputs "
+                  "(rows up to the first mismatch)", _zipf(1.0), 64, 4, 32000, 1.0, 4, greedy=True),
+] + [
+    ChainWorkload(f"ctl_B{b}_K{k}", f"spec-verify sampling B={b} V=151936 K={k} bf16 T=1, controlled "
+                  f"acceptance (draft row = target row w.p. 0.8, else an independent N(0,1) row)",
+                  _controlled(b, k), b, k, 151936, 1.0, 2)
+    for b, k in SWEEP
+]
 
 
 class SampleWorkload(Workload):
@@ -265,6 +480,9 @@ class SampleWorkload(Workload):
 
     def algorithmic_bytes(self, batch):
         return metric_bytes(batch.B, batch.K, batch.V)
+
+    def parity(self, batch, outs, n):
+        return sample_parity(batch, outs[0], outs[1], n)
 
     def oracle_call(self, batch, sl):
         import numpy as np
@@ -327,6 +545,9 @@ class GreedyWorkload(Workload):
 
         import oracle
         oracle.verify_greedy(batch.target[sl], batch.dtype, np.ascontiguousarray(batch.draft_tokens[sl]))
+
+    def parity(self, batch, outs, n):
+        return greedy_parity(batch, outs[0], outs[1], n)
 
     def device_setup(self, batch, dev):
         import torch
@@ -606,24 +827,67 @@ class DraftWorkload(Workload):
 
 
 WORKLOADS = {w.name: w for w in (SampleWorkload(), GreedyWorkload(), TreeWorkload(), TreeMaskWorkload(),
-                                 KvCommitWorkload(), StatsWorkload(), DraftWorkload())}
+                                 KvCommitWorkload(), StatsWorkload(), DraftWorkload(), *CHAIN_WORKLOADS)}
 
 
-def oracle_rate(wl: Workload, batch, budget_s: float, min_seqs: int):
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rate(wl: Workload, batch, budget_s: float, min_seqs: int, threads: int = 1):
     """The oracle, as it stands, over the batch's sequences (cycled, a few per
-    call) until about budget_s of CPU work; returns (units/s, sequences, seconds)."""
+    call) until about budget_s of wall time; `threads` host threads each run
+    their own calls (the oracle's C calls release the interpreter lock, so the
+    threads run on separate cores).  Returns (units/s, sequences, seconds)."""
     import oracle
     oracle.build()
+    oracle.lib()
     per_seq_units = wl.units(batch) / batch.B
-    done, t_used = 0, 0.0
-    while t_used < budget_s or done < min_seqs:
-        s0 = done % batch.B
-        sl = slice(s0, min(batch.B, s0 + wl.oracle_chunk()))
-        t0 = time.perf_counter()
-        wl.oracle_call(batch, sl)
-        t_used += time.perf_counter() - t0
-        done += sl.stop - sl.start
+    chunk = wl.oracle_chunk()
+    if threads <= 1:
+        done, t_used = 0, 0.0
+        while t_used < budget_s or done < min_seqs:
+            s0 = done % batch.B
+            sl = slice(s0, min(batch.B, s0 + chunk))
+            t0 = time.perf_counter()
+            wl.oracle_call(batch, sl)
+            t_used += time.perf_counter() - t0
+            done += sl.stop - sl.start
+        return done * per_seq_units / t_used, done, t_used
+    from concurrent.futures import ThreadPoolExecutor
+    slices = [slice(s0, min(batch.B, s0 + chunk)) for s0 in range(0, batch.B, chunk)]
+    done, k = 0, 0
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        while time.perf_counter() - t0 < budget_s or done < min_seqs:
+            rnd = [slices[(k + i) % len(slices)] for i in range(threads)]
+            k += threads
+            list(pool.map(lambda sl: wl.oracle_call(batch, sl), rnd))
+            done += sum(sl.stop - sl.start for sl in rnd)
+    t_used = time.perf_counter() - t0
     return done * per_seq_units / t_used, done, t_used
+
+
+def cpu_baseline(wl: Workload, batch, budget_s: float, outs=None, parity_seqs: int = 32):
+    """The CPU-baseline leg: the oracle on every host core (and on one, for
+    reference) over a bounded sample of the workload; when the GPU outputs are
+    given, the same leg compares the first sequences' outputs with the
+    oracle's (the parity block)."""
+    cores = host_cores()
+    rate, done, t_used = oracle_rate(wl, batch, budget_s, 4 * cores, threads=cores)
+    rate1, done1, t1 = oracle_rate(wl, batch, max(1.0, budget_s / 4), 2, threads=1)
+    cpu = {"value": rate, "unit": wl.unit, "cores": cores, "kind": "oracle",
+           "sample": f"{done} sequence verifications (the {batch.B} sequences of the same workload, cycled) "
+                     f"on {cores} threads, {t_used:.1f} s; single-threaded double-precision C oracle per call",
+           "value_1core": rate1, "sample_1core": f"{done1} sequence verifications on 1 thread, {t1:.1f} s"}
+    parity = None
+    if outs is not None:
+        n = min(batch.B, parity_seqs)
+        parity = wl.parity(batch, outs, n)
+    return cpu, parity
 
 
 def run_reference(args, wl: Workload, ws, rank):
@@ -631,21 +895,23 @@ def run_reference(args, wl: Workload, ws, rank):
     each step a bounded sample of the same workload."""
     if rank != 0:
         return
-    per_step = wl.oracle_chunk()
-    batch = wl.batch(list(range(per_step)))
+    cores = host_cores()
+    per_step = wl.oracle_chunk() * cores
+    batch = wl.batch(list(range(min(per_step, wl.per_rank))))
+    per_step = batch.B
     for _ in range(max(0, args.warmup)):
-        oracle_rate(wl, batch, 0.0, per_step)
+        oracle_rate(wl, batch, 0.0, per_step, threads=cores)
     t = 0.0
     for _ in range(args.steps):
-        _, _, dt = oracle_rate(wl, batch, 0.0, per_step)
+        _, _, dt = oracle_rate(wl, batch, 0.0, per_step, threads=cores)
         t += dt
     value = args.steps * wl.units(batch) / t
-    sample = f"{per_step} of the {wl.per_rank} sequences per step"
+    sample = f"{per_step} of the {wl.per_rank} sequences per step, on {cores} threads"
     line = {"impl": "reference", "metric": wl.metric, "value": value, "unit": wl.unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.oracle_dtype,
             "data": "synthetic", "config": wl.describe(),
-            "cpu_baseline": {"value": value, "unit": wl.unit, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": wl.unit, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -731,12 +997,11 @@ def run_ours(args, wl: Workload, ws, rank, local):
     alg = wl.algorithmic_bytes(batch)
     achieved = alg / (kern_avg_ms * 1e-3) / 1e9
     units = wl.units(batch)
-    cpu = None
+    cpu = parity = None
     if ws == 1:
-        cpu_rate, done, cpu_t = oracle_rate(wl, batch, args.cpu_budget, 4)
-        cpu = {"value": cpu_rate, "unit": wl.unit, "cores": 1, "kind": "oracle",
-               "sample": f"{done} sequence verifications (the {batch.B} sequences of the same workload, cycled), "
-                         f"single-threaded double-precision C oracle, {cpu_t:.1f} s"}
+        step()   # one more call: its outputs are the ones the parity block checks
+        torch.cuda.synchronize()
+        cpu, parity = cpu_baseline(wl, batch, args.cpu_budget, [o.cpu().numpy() for o in douts])
     cfg = wl.describe()
     cfg["parallelism"] = f"replicas over sequences x{ws}"
     cfg["algorithmic_bytes_per_step"] = alg
@@ -760,6 +1025,8 @@ def run_ours(args, wl: Workload, ws, rank, local):
         "clocks": clk,
         "cpu_baseline": cpu,
     }
+    if parity is not None:
+        line["parity"] = parity
     print(json.dumps(line), flush=True)
 
 
@@ -769,17 +1036,19 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="sample")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["sweep"], default="sample")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    wl = WORKLOADS[args.workload]
     ws, rank, local = dist_setup()
-    if args.impl == "reference":
-        run_reference(args, wl, ws, rank)
-    else:
-        run_ours(args, wl, ws, rank, local)
+    names = [f"ctl_B{b}_K{k}" for b, k in SWEEP] if args.workload == "sweep" else [args.workload]
+    for name in names:
+        wl = WORKLOADS[name]
+        if args.impl == "reference":
+            run_reference(args, wl, ws, rank)
+        else:
+            run_ours(args, wl, ws, rank, local)
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
