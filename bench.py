@@ -16,6 +16,10 @@ Other workloads (--workload):
           V=151936 bf16 T=1, B in {1, 8, 64, 512}, K in {4, 8}: each draft row is
           a copy of its target row with probability 0.8, else an independent row
   sweep   all eight ctl_B<B>_K<K> workloads in one run, one JSON line each
+  acceptance  spec_row_stats + spec_verify_sample on 5 x 10,000 one-draft
+          sequences (V=2048 f32) at graded draft noise: the acceptance rate
+          against sum min(p,q) and KL(q||p), and tokens per target pass against
+          K for alpha ~ 0.5 / 0.7 / 0.9 (controlled copies), in the JSON line
   greedy  spec_verify_greedy, B=256, V=128256, K=5, bf16; draft token t is the
           target row's argmax with probability 0.8
   tree    spec_verify_tree_greedy, B=128, N=64 nodes (BFS [4,3,2,1] truncated),
@@ -257,6 +261,10 @@ class Workload:
         the workload has no parity summary here)."""
         return None
 
+    def extra_report(self, batch) -> dict:
+        """Workload-specific measurements added to the JSON line."""
+        return {}
+
     def device_setup(self, batch, dev):
         """Returns (host inputs, device inputs they are copied to, step(),
         device outputs)."""
@@ -457,6 +465,129 @@ CHAIN_WORKLOADS = [
                   _controlled(b, k), b, k, 151936, 1.0, 2)
     for b, k in SWEEP
 ]
+
+
+class AcceptanceWorkload(Workload):
+    """The pages' acceptance measurement ("Speculative decoding: draft, verify,
+    repeat", step 4: acceptance rate against the divergence of the draft from
+    the verifier; "Speculative decoding and EAGLE", exercises: tokens per target
+    pass against K).  One step scores and verifies five batches of 10,000
+    one-draft sequences (V=2048 f32, T=1) whose drafts are the target plus
+    N(0, sigma^2) noise at graded sigma: spec_row_stats gives sum min(p,q) and
+    KL(q||p) per position, spec_verify_sample the accept decision."""
+    name = "acceptance"
+    metric = "draft positions scored and verified/s"
+    unit = "positions/s"
+    kernel = "row_stats_kernel + fused_sample_kernel (f32, V=2048)"
+    sources = ("common.cuh", "row_stats.cuh", "fused.cuh")
+    SIGMAS = (0.1, 0.3, 0.6, 1.0, 2.0)
+    NSEQ, VV = 10_000, 2048
+    COPY = (0.04, 0.42, 0.81)      # draft row = target row w.p. c (alpha ~ 0.5, 0.7, 0.9 at T=1)
+    KS = (1, 2, 3, 4, 5, 6, 7, 8)
+    per_rank = 10_000
+    launches_per_step = 2 * len(SIGMAS)
+
+    def describe(self):
+        return {"workload": "acceptance against KL(q||p): 5 batches of 10,000 one-draft sequences, V=2048 f32 "
+                            "T=1, draft = target + N(0, sigma^2), sigma in (0.1, 0.3, 0.6, 1.0, 2.0); per step "
+                            "spec_row_stats and spec_verify_sample on each batch",
+                "B": self.NSEQ, "V": self.VV, "K": 1, "temperature": 1.0,
+                "input_bytes": len(self.SIGMAS) * self.NSEQ * 3 * self.VV * 4,
+                "l2": "inputs (1.23 GB) larger than L2; no flush"}
+
+    class Batches(list):
+        """The five sigma batches; B = sequences per batch."""
+        B = 0
+
+    def batch(self, seqs):
+        from speculative_decoding_verification_52_gb300 import inputs as gen
+        out = self.Batches(gen.gaussian_chain_batch(len(seqs), self.VV, 1, sigma=s_, T=1.0, seed=52_600 + i)
+                           for i, s_ in enumerate(self.SIGMAS))
+        out.B = len(seqs)
+        return out
+
+    def units(self, batch):
+        return sum(b.B * b.K for b in batch)
+
+    def algorithmic_bytes(self, batch):
+        # statistics: target row 0 and draft row 0 of every sequence; verify:
+        # every row once plus one stopping target row
+        return sum(2 * b.B * b.K * b.V * 4 + metric_bytes(b.B, b.K, b.V, 4) for b in batch)
+
+    def oracle_chunk(self):
+        return 64
+
+    def oracle_call(self, batch, sl):
+        import numpy as np
+
+        import oracle
+        for b in batch:
+            oracle.row_stats(b.target[sl], "f32", b.draft[sl], "f32", False, 1.0)
+            oracle.verify_sample(b.target[sl], "f32", b.draft[sl], "f32", False,
+                                 np.ascontiguousarray(b.draft_tokens[sl]), np.ascontiguousarray(b.uniforms[sl]), 1.0)
+
+    def device_setup(self, batch, dev):
+        import torch
+
+        import speculative_decoding_verification_52_gb300 as sv
+        hs, ds, res = [], [], []
+        for b in batch:
+            h = [_pinned(b.target), _pinned(b.draft), _pinned(b.draft_tokens), _pinned(b.uniforms)]
+            hs += h
+            d = [x.to(dev) for x in h]
+            ds += d
+            r = dict(d=d, T=b.T, alpha=torch.empty((b.B, 1), dtype=torch.float32, device=dev),
+                     kl=torch.empty((b.B, 1), dtype=torch.float32, device=dev),
+                     tv=torch.empty((b.B, 1), dtype=torch.float32, device=dev),
+                     out=torch.empty((b.B, 2), dtype=torch.int32, device=dev),
+                     nacc=torch.empty((b.B,), dtype=torch.int32, device=dev),
+                     ws=sv.workspace(sv.spec_workspace_bytes(b.B, 1, b.V), dev))
+            res.append(r)
+        stream = torch.cuda.current_stream()
+        self._res = res
+
+        def step():
+            for r in res:
+                d = r["d"]
+                sv.spec_row_stats(d[0], d[1], r["T"], alpha=r["alpha"], kl=r["kl"], tv=r["tv"], stream=stream)
+                sv.spec_verify_sample(d[0], d[1], d[2], d[3], r["T"], out_tokens=r["out"], num_accepted=r["nacc"],
+                                      workspace_buf=r["ws"], stream=stream)
+        outs = [x for r in res for x in (r["alpha"], r["kl"], r["nacc"])]
+        return hs, ds, step, outs
+
+    def extra_report(self, batch):
+        """The acceptance curve from the last step's outputs, and tokens per
+        target pass against K on controlled-copy batches (2,000 sequences,
+        V=1024 f32, run once here)."""
+        import numpy as np
+        import torch
+
+        import speculative_decoding_verification_52_gb300 as sv
+        from speculative_decoding_verification_52_gb300 import inputs as gen
+        torch.cuda.synchronize()
+        curve = []
+        for s_, r in zip(self.SIGMAS, self._res):
+            a = r["alpha"].cpu().numpy()[:, 0]
+            kl = r["kl"].cpu().numpy()[:, 0]
+            acc = (r["nacc"].cpu().numpy() >= 1).astype(np.float64)
+            m = float(a.mean())
+            curve.append({"sigma": s_, "mean_alpha": m, "mean_kl": float(kl.mean()),
+                          "accept_rate": float(acc.mean()), "se": float(np.sqrt(m * (1 - m) / len(acc)))})
+        dev = torch.device("cuda", torch.cuda.current_device())
+        tpp = []
+        for c in self.COPY:
+            for k in self.KS:
+                b = gen.controlled_chain_batch(2000, k, 1024, c, 1.0, seed=52_650 + k)
+                t = torch.from_numpy(b.target).to(dev)
+                d = torch.from_numpy(b.draft).to(dev)
+                alpha, _, _ = sv.spec_row_stats(t, d, b.T)
+                _, n = sv.spec_verify_sample(t, d, torch.from_numpy(b.draft_tokens).to(dev),
+                                             torch.from_numpy(b.uniforms).to(dev), b.T)
+                al = float(alpha.mean().item())
+                tok = n.cpu().numpy().astype(np.float64) + 1.0
+                tpp.append({"copy_prob": c, "K": k, "alpha": al, "tokens_per_pass": float(tok.mean()),
+                            "closed_form": (1 - al ** (k + 1)) / (1 - al), "se": float(tok.std() / np.sqrt(len(tok)))})
+        return {"acceptance_curve": curve, "tokens_per_pass": tpp}
 
 
 class SampleWorkload(Workload):
@@ -827,7 +958,8 @@ class DraftWorkload(Workload):
 
 
 WORKLOADS = {w.name: w for w in (SampleWorkload(), GreedyWorkload(), TreeWorkload(), TreeMaskWorkload(),
-                                 KvCommitWorkload(), StatsWorkload(), DraftWorkload(), *CHAIN_WORKLOADS)}
+                                 KvCommitWorkload(), StatsWorkload(), DraftWorkload(), AcceptanceWorkload(),
+                                 *CHAIN_WORKLOADS)}
 
 
 def host_cores() -> int:
@@ -957,7 +1089,7 @@ def run_ours(args, wl: Workload, ws, rank, local):
     # the same steps again with the library's timing hooks on (CUDA events
     # around the kernels of each call: part 1 = the sweep, or the whole fused
     # kernel; part 2 = the finishing kernel, none when fused) for the roofline
-    sv.spec_profile_begin(args.steps)
+    sv.spec_profile_begin(args.steps * wl.launches_per_step)
     for _ in range(args.steps):
         step()
     torch.cuda.synchronize()
@@ -995,7 +1127,7 @@ def run_ours(args, wl: Workload, ws, rank, local):
     peaks, src = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     alg = wl.algorithmic_bytes(batch)
-    achieved = alg / (kern_avg_ms * 1e-3) / 1e9
+    achieved = alg / wl.launches_per_step / (kern_avg_ms * 1e-3) / 1e9   # bytes per launch / launch time
     units = wl.units(batch)
     cpu = parity = None
     if ws == 1:
@@ -1011,7 +1143,8 @@ def run_ours(args, wl: Workload, ws, rank, local):
             "frac": achieved / hbm, "peak_source": f"{src} hbm_gbs (burst copy)",
             "traffic": profiled_traffic(wl.summary, wl.sources), "algorithmic_bytes": alg, "avg_launch_ms": kern_avg_ms}
     if wl.launches_per_step > 1:
-        roof["finish_avg_ms"] = fin_avg_ms
+        roof["launches_per_step"] = wl.launches_per_step
+    extra = wl.extra_report(batch)
     line = {
         "metric": wl.metric, "value": ws * units / (ms * 1e-3), "unit": wl.unit, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -1027,6 +1160,8 @@ def run_ours(args, wl: Workload, ws, rank, local):
     }
     if parity is not None:
         line["parity"] = parity
+    if extra:
+        line.update(extra)
     print(json.dumps(line), flush=True)
 
 

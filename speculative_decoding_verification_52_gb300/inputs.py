@@ -160,6 +160,42 @@ def gaussian_chain(B: int, V: int, K: int, sigma: float, T: float, dtype: str,
                       meta=dict(sigma=sigma, seed=seed, seqs=seqs))
 
 
+def gaussian_chain_batch(B: int, V: int, K: int, sigma: float, T: float, seed: int,
+                         name: str = "") -> ChainBatch:
+    """gaussian_chain's recipe (target ~ N(0,1), draft = target + N(0, sigma^2),
+    draft tokens sampled from softmax(draft/T) by Gumbel-max), f32, drawn
+    from one generator for the whole batch (vectorised; large measurement
+    batches, where a subset need not reproduce the full batch's rows)."""
+    rng = np.random.default_rng([int(seed), 7])
+    z = rng.standard_normal((B, K + 1, V))
+    y = z[:, :K] + sigma * rng.standard_normal((B, K, V))
+    tgt = z.astype(np.float32)
+    dft = y.astype(np.float32)
+    g = -np.log(-np.log(np.maximum(rng.random((B, K, V)), 1e-300)))
+    tok = np.argmax(dft.astype(np.float64) / T + g, axis=-1).astype(np.int32)
+    uni = rng.random((B, K + 1, 2), dtype=np.float32)
+    return ChainBatch(B, K, V, T, F32, tgt, dft, False, tok, uni, name=name,
+                      meta=dict(sigma=sigma, seed=seed))
+
+
+def controlled_chain_batch(B: int, K: int, V: int, copy_prob: float, T: float, seed: int,
+                           name: str = "") -> ChainBatch:
+    """config_controlled's recipe (target rows ~ N(0,1); each draft row a copy of
+    its target row with probability copy_prob, else an independent N(0,1) row;
+    tokens sampled from the draft), f32, drawn from one generator for the whole
+    batch (vectorised)."""
+    rng = np.random.default_rng([int(seed), 11])
+    tgt = rng.standard_normal((B, K + 1, V)).astype(np.float32)
+    indep = rng.standard_normal((B, K, V)).astype(np.float32)
+    copied = rng.random((B, K)) < copy_prob
+    dft = np.where(copied[..., None], tgt[:, :K], indep)
+    g = -np.log(-np.log(np.maximum(rng.random((B, K, V)), 1e-300)))
+    tok = np.argmax(dft.astype(np.float64) / T + g, axis=-1).astype(np.int32)
+    uni = rng.random((B, K + 1, 2), dtype=np.float32)
+    return ChainBatch(B, K, V, T, F32, tgt, np.ascontiguousarray(dft), False, tok, uni, name=name,
+                      meta=dict(copied=copied, copy_prob=copy_prob, seed=seed))
+
+
 def config_tiny(trials: int = 200_000, seed: int = 52_100, V: int = 8, K: int = 4,
                 T: float = 1.0, sigma: float = 0.5) -> ChainBatch:
     """Tiny exactness workload: one (target, draft) pair of fp32 logit sets
@@ -374,6 +410,7 @@ def config_tree(B: int = 128, V: int = 128256, branching=(4, 3, 2, 1), N: int = 
 __all__ = [
     "F32", "BF16", "ChainBatch", "TreeBatch", "SIGMA_B256_V128K", "config_greedy",
     "f32_to_bf16_bits", "bf16_bits_to_f64", "as_f64", "gaussian_chain",
-    "config_tiny", "config_zipf", "config_headline", "config_controlled",
+    "config_tiny", "config_zipf", "config_headline", "config_controlled", "gaussian_chain_batch",
+    "controlled_chain_batch",
     "config_tree", "config_tree_draft", "bfs_tree", "tree_depths", "config_tree_masks", "KvBatch", "config_kv_commit",
 ]
