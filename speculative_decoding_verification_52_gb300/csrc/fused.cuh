@@ -1064,10 +1064,13 @@ __device__ void fu_consumer(const FusedArgs& a, unsigned char* ring, FuShared& s
       __threadfence_block();
       if (d.kind == KIND_SWEEP) {
         *reinterpret_cast<volatile int*>(&sh.slot_unit[d.slot]) = d.unit + 1;
+        mbar_arrive(&sh.empty[cur]);
       } else {
+        // the stage first: the release reduction waits until the block sums
+        // are visible device-wide, and the ring should not wait with it
+        mbar_arrive(&sh.empty[cur]);
         red_release_add_u32(fu_cnt2(a, d.b), 1u);
       }
-      mbar_arrive(&sh.empty[cur]);
     } else if (lane == 0) {
       mbar_arrive(&sh.empty[cur]);
     }

@@ -545,17 +545,18 @@ spec_status_t dispatch_sample(const DevInfo& di, int dev, const void* target, sp
 // greedy tree, pruned (one persistent kernel)
 // ---------------------------------------------------------------------------
 // Workspace of the pruned tree kernel:
-//   [TrCtl (128 B) | cnt[B*N] | fifo[B*(N-1)*S]]   zeroed per call
+//   [TrCtl (128 B) | cnt[B*N] | fifo[B*(N-1)*S] | sdone[B]]   zeroed per call
 //   [part[B*N*S*8]]
 struct TreeLayout {
-  size_t fifo_off, zero_bytes, part_off, total;
+  size_t fifo_off, sdone_off, zero_bytes, part_off, total;
 };
 TreeLayout tree_layout(int B, int N, int S) {
   TreeLayout l{};
   const size_t nodes = static_cast<size_t>(B) * static_cast<size_t>(N);
   const size_t qcap = static_cast<size_t>(B) * static_cast<size_t>(N - 1) * static_cast<size_t>(S);
   l.fifo_off = align_up(128 + sizeof(unsigned) * nodes, 128);
-  l.zero_bytes = l.fifo_off + sizeof(unsigned) * qcap;
+  l.sdone_off = l.fifo_off + sizeof(unsigned) * qcap;
+  l.zero_bytes = l.sdone_off + sizeof(unsigned) * static_cast<size_t>(B);
   l.part_off = align_up(l.zero_bytes, 256);
   l.total = align_up(l.part_off + nodes * static_cast<size_t>(S) * TR_CW * sizeof(float2), 256);
   return l;
@@ -616,6 +617,7 @@ spec_status_t run_tree_pruned(const DevInfo& di, int dev, const void* target, co
   a.ctl = reinterpret_cast<TrCtl*>(w);
   a.cnt = reinterpret_cast<unsigned*>(w + 128);
   a.fifo = reinterpret_cast<unsigned*>(w + lay.fifo_off);
+  a.sdone = reinterpret_cast<unsigned*>(w + lay.sdone_off);
   a.part = reinterpret_cast<float2*>(w + lay.part_off);
   a.out_tokens = out;
   a.num_accepted = nacc;

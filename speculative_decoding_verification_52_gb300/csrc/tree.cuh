@@ -30,8 +30,13 @@
 //
 // Chain mode runs the greedy chain rule ("The exactness rule", greedy case)
 // through the same machinery: node t is the drafted position t (parent t - 1,
-// token x_{t-1}), so rows after the first mismatch are never read, and a draft
-// token outside [0, V) makes the sequence invalid.
+// token x_{t-1}), and a draft token outside [0, V) makes the sequence invalid.
+// A chain's levels depend on one another, so chain mode sweeps TR_AHEAD rows
+// ahead: rows 0..TR_AHEAD of every sequence are implicit units, and when row t
+// resolves with x_t == argmax (position t+1 accepted) row t+1+TR_AHEAD is
+// queued, before the rows between are known to be needed.  At most TR_AHEAD
+// rows past the first mismatch are read; producers skip queued rows of
+// sequences that have already finished.
 //
 // The tree topology (parents[]) is checked and its depths computed once per
 // CTA in shared memory.  Every wait is bounded in time; a timeout sets an error
@@ -51,6 +56,7 @@ constexpr int TR_NSTAGE = 4;
 constexpr int TR_CTAS_PER_SM = 3;
 constexpr int TR_MAX_N = 1024;                    // node bits: 32 lanes x 32 words
 constexpr int TR_MAX_SEQ = 4;                     // sequences per finisher warp
+constexpr int TR_AHEAD = 1;                       // chain mode: rows swept ahead of the last resolved one
 
 struct TrCtl {                   // zeroed before every call (96 bytes reserved)
   unsigned err;                  // a wait timed out
@@ -74,6 +80,7 @@ struct TreeArgs {
   TrCtl* ctl;
   unsigned* cnt;                 // [B * N] units completed per node
   unsigned* fifo;                // [qcap] unit id + 1, 0 = not yet written
+  unsigned* sdone;               // [B] 1 once the sequence's outputs are written (chain look-ahead)
   float2* part;                  // [B * N * S * TR_CW] warp partials
   int32_t* out_tokens;           // [B, max_depth + 1]
   int32_t* num_accepted;         // [B]
@@ -181,7 +188,9 @@ __device__ void tr_producer(const TreeArgs& a, unsigned char* ring, TrShared& sh
     if (++stage == TR_NSTAGE) { stage = 0; phase ^= 1u; }
   };
 
+  // implicit units: node 0 of every sequence, and in chain mode nodes 1..TR_AHEAD too
   const unsigned roots = static_cast<unsigned>(a.B) * static_cast<unsigned>(a.S);
+  const unsigned implicit = (a.chain ? static_cast<unsigned>(min(a.N, TR_AHEAD + 1)) : 1u) * roots;
   const unsigned B = static_cast<unsigned>(a.B);
   bool ok = sh.topo_ok != 0;
   unsigned k = ok ? atomicAdd(&a.ctl->qhead, 1u) : 0u;
@@ -189,11 +198,13 @@ __device__ void tr_producer(const TreeArgs& a, unsigned char* ring, TrShared& sh
     const unsigned kc = k;
     k = atomicAdd(&a.ctl->qhead, 1u);   // next claim, in flight while this unit streams
     unsigned uid;
-    if (kc < roots) {
-      uid = (kc / a.S * a.N) * a.S + kc % a.S;   // (b, node 0, slice j)
+    if (kc < implicit) {
+      const unsigned node = kc / roots;
+      const unsigned r = kc - node * roots;
+      uid = (r / a.S * a.N + node) * a.S + r % a.S;   // (b, node, slice j)
     } else {
       // wait until position kc is written, or every sequence is finished
-      const unsigned q = kc - roots;
+      const unsigned q = kc - implicit;
       const uint64_t t0 = global_ns();
       unsigned v = 0;
       for (;;) {
@@ -207,6 +218,8 @@ __device__ void tr_producer(const TreeArgs& a, unsigned char* ring, TrShared& sh
       }
       if (v == 0u) break;
       uid = v - 1u;
+      // a queued look-ahead row of a chain that has already finished is not needed
+      if (a.chain && ld_relaxed_u32(a.sdone + uid / a.S / a.N) != 0u) continue;
     }
     const unsigned row = uid / a.S;   // b * N + node
     const int j = static_cast<int>(uid - row * a.S);
@@ -281,11 +294,16 @@ __device__ void tr_consumer(const TreeArgs& a, unsigned char* ring, TrShared& sh
       __threadfence_block();
       const int prev = atomicAdd(&sh.unit_cnt[cur], 1);
       if (prev == TR_CW - 1) {
-        sh.unit_cnt[cur] = 0;
+        sh.unit_cnt[cur] = 0;   // (before the stage is released: its next unit counts from zero)
         __threadfence_block();
+        // The stage is released first: the release reduction below waits
+        // until the unit's partials are visible device-wide, and the ring
+        // should not wait with it.
+        mbar_arrive(&sh.empty[cur]);
         red_release_add_u32(a.cnt + d.uid / a.S, 1u);
+      } else {
+        mbar_arrive(&sh.empty[cur]);
       }
-      mbar_arrive(&sh.empty[cur]);
     }
     __syncwarp();
   }
@@ -359,7 +377,10 @@ __device__ void tr_finisher(const TreeArgs& a, TrShared& sh, int lane) {
         tr_write_invalid(a, seq[s], -1, lane);
         live[s] = false;
         --nlive;
-        if (lane == 0) atomicAdd(&a.ctl->seqs_done, 1u);
+        if (lane == 0) {
+          a.sdone[seq[s]] = 1u;
+          atomicAdd(&a.ctl->seqs_done, 1u);
+        }
       }
     }
   }
@@ -402,7 +423,10 @@ __device__ void tr_finisher(const TreeArgs& a, TrShared& sh, int lane) {
           tr_write_invalid(a, b, -1, lane);
           live[s] = false;
           --nlive;
-          if (lane == 0) atomicAdd(&a.ctl->seqs_done, 1u);
+          if (lane == 0) {
+            if (a.chain) a.sdone[b] = 1u;
+            atomicAdd(&a.ctl->seqs_done, 1u);
+          }
           progress = true;
           break;
         }
@@ -413,19 +437,24 @@ __device__ void tr_finisher(const TreeArgs& a, TrShared& sh, int lane) {
           bestg[s] = g;
         }
         // children of `node` whose token equals g are accepted; their units
-        // are appended to the FIFO (c % 32 == lane, so each lane owns its bits)
+        // are appended to the FIFO (c % 32 == lane, so each lane owns its bits).
+        // In chain mode the accepted child's row is already queued (TR_AHEAD
+        // rows ahead), so the row TR_AHEAD beyond it is appended instead.
         for (int c0 = (node + 1) & ~31; c0 < a.N; c0 += 32) {
           const int c = c0 + lane;
           const bool take = c > node && c < a.N && sh.par[c] == node && tr_token(a, b, c) == g;
           const unsigned tb = __ballot_sync(0xffffffffu, take);
           if (!tb) continue;
           if (take) accm[s] |= 1u << (c >> 5);
+          const bool q_this = take && (!a.chain || c + TR_AHEAD < a.N);
+          const unsigned qb = __ballot_sync(0xffffffffu, q_this);
+          if (!qb) continue;
           unsigned base = 0;
-          if (lane == 0) base = atomicAdd(&a.ctl->qtail, static_cast<unsigned>(__popc(tb)) * S);
+          if (lane == 0) base = atomicAdd(&a.ctl->qtail, static_cast<unsigned>(__popc(qb)) * S);
           base = __shfl_sync(0xffffffffu, base, 0);
-          if (take) {
-            const unsigned r = __popc(tb & ((1u << lane) - 1u));
-            const unsigned u0 = (static_cast<unsigned>(b) * a.N + c) * S;
+          if (q_this) {
+            const unsigned r = __popc(qb & ((1u << lane) - 1u));
+            const unsigned u0 = (static_cast<unsigned>(b) * a.N + (a.chain ? c + TR_AHEAD : c)) * S;
             for (unsigned j = 0; j < S; ++j) {
               const unsigned q = base + r * S + j;
               if (q < a.qcap) a.fifo[q] = u0 + j + 1u;
@@ -440,7 +469,10 @@ __device__ void tr_finisher(const TreeArgs& a, TrShared& sh, int lane) {
         tr_write_path(a, sh, b, best[s], bestg[s], lane);
         live[s] = false;
         --nlive;
-        if (lane == 0) atomicAdd(&a.ctl->seqs_done, 1u);
+        if (lane == 0) {
+          if (a.chain) a.sdone[b] = 1u;
+          atomicAdd(&a.ctl->seqs_done, 1u);
+        }
         progress = true;
       }
     }

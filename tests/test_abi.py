@@ -37,11 +37,12 @@ def test_workspace_sizes(L):
     fused = al(part + B_ * (2 * K_ + 1) * 63 * 16, 256)
     assert L.spec_workspace_bytes(B_, K_, V_) == fused   # larger than the greedy chain's pruned layout here
     fused1 = al(al(al(al(32 + 32, 32) + 32, 16) + 4, 16) + 16, 256)
-    assert L.spec_workspace_bytes(1, 0, 8) == max(fused1, al(256 + 64, 256))
+    # the greedy chain's pruned layout: control block + counters + FIFO + done flags, then partials
+    assert L.spec_workspace_bytes(1, 0, 8) == max(fused1, al(al(256 + 4, 256) + 64, 256))
     # tree: max(full sweep partials, pruned-kernel layout with at most ceil(V/4096) slices)
     nodes, smax = 128 * 64, -(-128256 // 4096)
     fifo = al(128 + 4 * nodes, 128)
-    pruned = al(al(fifo + 4 * 128 * 63 * smax, 256) + nodes * smax * 8 * 8, 256)
+    pruned = al(al(fifo + 4 * 128 * 63 * smax + 4 * 128, 256) + nodes * smax * 8 * 8, 256)
     assert L.spec_tree_workspace_bytes(128, 64, 128256) == max(128 * 64 * 63 * 8, pruned)
     for bad in [(-1, 4, 10), (1, -1, 10), (1, 32, 10), (1, 4, 0)]:
         assert L.spec_workspace_bytes(*bad) == 0
