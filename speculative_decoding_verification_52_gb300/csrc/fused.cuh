@@ -142,6 +142,7 @@ struct FuShared {
   int res_want;                  // sequence of the producer's next residual unit (-1: none)
   int res_have;                  // sequence whose readiness word is in res_word (-1: none)
   int grid_ready;                // the control block is cleared on every CTA (set by the merger warp)
+  float4 scan_scratch[32];       // the finisher's per-lane row shares during an accept scan
   int abort;
 };
 
@@ -457,46 +458,88 @@ __device__ __forceinline__ float4 merge_unit(float2 p, int lane, float c) {
   return make_float4(nan ? __int_as_float(0x7fc00000) : M, hi, lo, 0.f);
 }
 
-// Merge the S unit partials of row r of sequence b (one lane): online
-// float-float accumulation relative to the running maximum.  Row r lands in
-// slot r >> 5 of this lane (lane r & 31).
-__device__ __forceinline__ void merge_row(const FusedArgs& a, int b, int r, float (&Ar)[2], FF (&Sr)[2],
-                                          int (&st)[2]) {
-  const float4* up = a.part + (static_cast<long long>(b) * a.RB + r) * a.S;
-  float M = kNegInf, hi = 0.f, lo = 0.f;
-  bool bad = false;
-  const float c = a.c;
-#pragma unroll 4
-  for (int j = 0; j < a.S; ++j) {
-    const float4 u = __ldcg(up + j);
-    if (u.x != u.x) {
-      bad = true;
-      continue;
-    }
-    if (u.x == kNegInf) continue;
-    if (u.x > M) {
-      if (M != kNegInf) {
-        const float f = exp2f(__fmul_rn(M, c) - __fmul_rn(u.x, c));
-        const float h = hi * f;
-        lo = fmaf(hi, f, -h) + lo * f;
-        hi = h;
-      }
-      M = u.x;
-    }
-    const float f = exp2f(__fmul_rn(u.x, c) - __fmul_rn(M, c));
-    const float h = u.y * f;
-    const float2 t = two_sum(hi, h);
-    hi = t.x;
-    lo += t.y + fmaf(u.y, f, -h) + u.z * f;
+// Online float-float accumulation of normaliser partials (m, hi, lo): the
+// running maximum M and the sum hi + lo relative to fl(M*c).  A NaN partial
+// poisons the accumulation; partials of only -inf elements add nothing.
+struct RowAcc {
+  float M, hi, lo;
+  bool bad;
+};
+__device__ __forceinline__ void row_acc_add(RowAcc& s, float4 u, float c) {
+  if (u.x != u.x) {
+    s.bad = true;
+    return;
   }
-  const FF acc = ff_norm(hi, lo);
-  Ar[r >> 5] = (bad || M == kNegInf) ? 0.f : __fmul_rn(M, c);
-  Sr[r >> 5] = acc;
-  st[r >> 5] = bad ? 2 : (M == kNegInf ? 1 : ((isfinite(acc.hi) && acc.hi > 0.f) ? 0 : 1));
+  if (u.x == kNegInf) return;
+  if (u.x > s.M) {
+    if (s.M != kNegInf) {
+      const float f = exp2f(__fmul_rn(s.M, c) - __fmul_rn(u.x, c));
+      const float h = s.hi * f;
+      s.lo = fmaf(s.hi, f, -h) + s.lo * f;
+      s.hi = h;
+    }
+    s.M = u.x;
+  }
+  const float f = exp2f(__fmul_rn(u.x, c) - __fmul_rn(s.M, c));
+  const float h = u.y * f;
+  const float2 t = two_sum(s.hi, h);
+  s.hi = t.x;
+  s.lo += t.y + fmaf(u.y, f, -h) + u.z * f;
+}
+
+// The row's scale, sum and state (0 valid, 1 invalid: no finite entry or a
+// non-positive or infinite sum, 2 poisoned) from its accumulation.
+__device__ __forceinline__ void row_acc_result(const RowAcc& s, float c, float& A, FF& S, int& st) {
+  const FF acc = ff_norm(s.hi, s.lo);
+  A = (s.bad || s.M == kNegInf) ? 0.f : __fmul_rn(s.M, c);
+  S = acc;
+  st = s.bad ? 2 : (s.M == kNegInf ? 1 : ((isfinite(acc.hi) && acc.hi > 0.f) ? 0 : 1));
+}
+
+// Accumulate the unit partials j0, j0 + step, ... of one row (one lane).
+__device__ __forceinline__ RowAcc merge_share(const float4* up, int j0, int step, int S, float c) {
+  RowAcc s{kNegInf, 0.f, 0.f, false};
+#pragma unroll 4
+  for (int j = j0; j < S; j += step) row_acc_add(s, __ldcg(up + j), c);
+  return s;
+}
+
+// Merge the unit partials of every row of sequence b.  Small batches split
+// rows into many slices (one ring stage each), so with at most 16 rows of more
+// than 4 slices each row gets lpr = min(32 / rows, S) lanes that accumulate a
+// strided share of its slices; the shares meet in the scratch in shared
+// memory, where lane r combines row r's.  Otherwise lane r merges rows r and
+// r + 32 alone.  Row r lands in slot r >> 5 of lane r & 31.  (The kernel's
+// sweep rate proved sensitive to the size of this rarely run code, so both
+// forms share one accumulation routine.)
+__device__ __forceinline__ void merge_rows(const FusedArgs& a, int b, int lane, float4* scratch, float (&Ar)[2],
+                                           FF (&Sr)[2], int (&st)[2]) {
+  const int RB = a.RB, S = a.S;
+  const float c = a.c;
+  const int lpr = (RB <= 16 && S > 4) ? max(1, min(32 / RB, S)) : 1;
+  if (lpr == 1) {
+    for (int r = lane; r < RB; r += 32) {
+      const RowAcc s = merge_share(a.part + (static_cast<long long>(b) * RB + r) * S, 0, 1, S, c);
+      row_acc_result(s, c, Ar[r >> 5], Sr[r >> 5], st[r >> 5]);
+    }
+    return;
+  }
+  const int r = lane / lpr;
+  RowAcc s{kNegInf, 0.f, 0.f, false};
+  if (r < RB) s = merge_share(a.part + (static_cast<long long>(b) * RB + r) * S, lane - r * lpr, lpr, S, c);
+  // a poisoned share travels as a NaN maximum
+  scratch[lane] = make_float4(s.bad ? __int_as_float(0x7fc00000) : s.M, s.hi, s.lo, 0.f);
+  __syncwarp();
+  if (lane < RB) {
+    RowAcc t{kNegInf, 0.f, 0.f, false};
+    for (int k = 0; k < lpr; ++k) row_acc_add(t, scratch[lane * lpr + k], c);
+    row_acc_result(t, c, Ar[0], Sr[0], st[0]);
+  }
+  __syncwarp();
 }
 
 template <class TP, class TQ, bool PROBS>
-__device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInputs& in) {
+__device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInputs& in, float4* scratch) {
   const int K = a.K, W = K + 1, V = a.V;
   const int x = in.x;
   const float u0 = in.u0;
@@ -504,8 +547,7 @@ __device__ void finish_scan(const FusedArgs& a, int b, int lane, const ScanInput
   FF Sr[2] = {FF{0.f, 0.f}, FF{0.f, 0.f}};
   int st[2] = {1, 1};
   // lane r merges row r (and row r + 32 when there are more than 32 rows)
-  if (lane < a.RB) merge_row(a, b, lane, Ar, Sr, st);
-  if (lane + 32 < a.RB) merge_row(a, b, lane + 32, Ar, Sr, st);
+  merge_rows(a, b, lane, scratch, Ar, Sr, st);
 
   // lane t tests position t
   const int t = lane;
@@ -1201,7 +1243,7 @@ __device__ void fu_finisher(const FusedArgs& a, FuShared& sh, int lane) {
     const unsigned need_scan = per_seq + (static_cast<int>(bs) == a.debug_stall_b ? 1u : 0u);
     if (bs < static_cast<unsigned>(a.B) && v_scan == need_scan) {
       __threadfence();
-      finish_scan<TP, TQ, PROBS>(a, static_cast<int>(bs), lane, in);
+      finish_scan<TP, TQ, PROBS>(a, static_cast<int>(bs), lane, in, sh.scan_scratch);
       bs += G;
       if (bs < static_cast<unsigned>(a.B)) in = scan_inputs<TP, TQ, PROBS>(a, static_cast<int>(bs), lane);
       progress = true;
