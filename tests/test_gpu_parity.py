@@ -140,9 +140,12 @@ def test_sample_headline_full(orc):
     st = {}
     gu.compare_sample(out, n, ref, st)
     # at V = 128256 a token's residual mass is ~1e-5 of the total, so about one
-    # draw in ten lands within 1e-6 of a CDF boundary; nearly all still agree
+    # draw in eight lands within 1e-6 of a CDF boundary (the oracle flags 31 of
+    # these 256 sequences, all at the draw, none at an accept test); nearly all
+    # still agree
     print("headline flagged:", st)
-    assert st["flagged"] < 0.25 * b.B
+    assert st["flagged"] <= 0.15 * b.B
+    assert int((ref["near_accept"] >= 0).sum()) == 0
     assert st["flagged_mismatch"] <= 2
     acc = (n.astype(np.float64)).mean() / b.K
     assert 0.4 < acc < 0.95
