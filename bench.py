@@ -238,6 +238,7 @@ class Workload:
     launches_per_step = 1
     dtype = "f32"            # what the path computes in
     oracle_dtype = "f64"
+    seq_noun = "sequence verifications"   # what one oracle sequence of the batch is
 
     def describe(self) -> dict:
         raise NotImplementedError
@@ -765,6 +766,7 @@ class TreeMaskWorkload(Workload):
     unit = "rows/s"
     summary = "tree_mask_kernel_b4096_n256.md"
     kernel = "tree_mask_reg_kernel<8>"
+    seq_noun = "trees masked"
     sources = ("tree_mask.cuh",)
     dtype = oracle_dtype = "u32"
     per_rank = 4096
@@ -819,6 +821,7 @@ class KvCommitWorkload(Workload):
     unit = "entries/s"
     summary = "kv_commit_kernel_b256_e64k.md"
     kernel = "kv_commit_kernel"
+    seq_noun = "chains committed"
     sources = ("kv_commit.cuh",)
     dtype = oracle_dtype = "u8"
 
@@ -864,6 +867,7 @@ class StatsWorkload(Workload):
     unit = "positions/s"
     summary = "row_stats_kernel_b256_v128256_k5_bf16.md"
     kernel = "row_stats_kernel<bf16, bf16 logits>"
+    seq_noun = "sequences' statistics"
     sources = ("common.cuh", "row_stats.cuh")
 
     def describe(self):
@@ -906,7 +910,8 @@ class DraftWorkload(Workload):
     metric = "drafted tree nodes/s"
     unit = "nodes/s"
     summary = "tree_draft_kernel_b128_n64_v128256_bf16.md"
-    kernel = "tree_draft_kernel<bf16, 4>"
+    kernel = "tree_draft_kernel<bf16>"
+    seq_noun = "trees drafted"
     sources = ("common.cuh", "tree_draft.cuh")
     per_rank = TREE_B
 
@@ -1013,9 +1018,9 @@ def cpu_baseline(wl: Workload, batch, budget_s: float, outs=None, parity_seqs: i
     rate, done, t_used = oracle_rate(wl, batch, budget_s, 4 * cores, threads=cores)
     rate1, done1, t1 = oracle_rate(wl, batch, max(1.0, budget_s / 4), 2, threads=1)
     cpu = {"value": rate, "unit": wl.unit, "cores": cores, "kind": "oracle",
-           "sample": f"{done} sequence verifications (the {batch.B} sequences of the same workload, cycled) "
+           "sample": f"{done} {wl.seq_noun} (the {batch.B} of the same workload, cycled) "
                      f"on {cores} threads, {t_used:.1f} s; single-threaded double-precision C oracle per call",
-           "value_1core": rate1, "sample_1core": f"{done1} sequence verifications on 1 thread, {t1:.1f} s"}
+           "value_1core": rate1, "sample_1core": f"{done1} {wl.seq_noun} on 1 thread, {t1:.1f} s"}
     parity = None
     if outs is not None:
         n = min(batch.B, parity_seqs)

@@ -739,9 +739,9 @@ spec_status_t launch_row_stats(int dev, const RowStatsArgs& a, cudaStream_t st) 
 // ---------------------------------------------------------------------------
 // top-k tree drafting
 // ---------------------------------------------------------------------------
-template <class T, int KM>
+template <class T>
 spec_status_t launch_tree_draft(int dev, unsigned grid, size_t smem, const TreeDraftArgs& a, cudaStream_t st) {
-  auto kern = tree_draft_kernel<T, KM>;
+  auto kern = tree_draft_kernel<T>;
   if (!once_per_device(dev, [&] {
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TD_NS * TD_STAGE) ==
                cudaSuccess;
@@ -1135,25 +1135,9 @@ spec_status_t spec_tree_draft(const void* draft_logits, spec_dtype_t draft_dtype
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const unsigned grid = static_cast<unsigned>(static_cast<long long>(B) * N);
     prof_mark(0, st);
-    const int km = max_children <= 1 ? 1 : max_children <= 2 ? 2 : max_children <= 4 ? 4 : max_children <= 8 ? 8 : 16;
     const size_t smem = a.vec ? static_cast<size_t>(TD_NS) * TD_STAGE : 0;
-    if (draft_dtype == SPEC_BF16) {
-      switch (km) {
-        case 1: s = launch_tree_draft<BF16T, 1>(dev, grid, smem, a, st); break;
-        case 2: s = launch_tree_draft<BF16T, 2>(dev, grid, smem, a, st); break;
-        case 4: s = launch_tree_draft<BF16T, 4>(dev, grid, smem, a, st); break;
-        case 8: s = launch_tree_draft<BF16T, 8>(dev, grid, smem, a, st); break;
-        default: s = launch_tree_draft<BF16T, 16>(dev, grid, smem, a, st); break;
-      }
-    } else {
-      switch (km) {
-        case 1: s = launch_tree_draft<F32T, 1>(dev, grid, smem, a, st); break;
-        case 2: s = launch_tree_draft<F32T, 2>(dev, grid, smem, a, st); break;
-        case 4: s = launch_tree_draft<F32T, 4>(dev, grid, smem, a, st); break;
-        case 8: s = launch_tree_draft<F32T, 8>(dev, grid, smem, a, st); break;
-        default: s = launch_tree_draft<F32T, 16>(dev, grid, smem, a, st); break;
-      }
-    }
+    s = draft_dtype == SPEC_BF16 ? launch_tree_draft<BF16T>(dev, grid, smem, a, st)
+                                 : launch_tree_draft<F32T>(dev, grid, smem, a, st);
     if (s != SPEC_OK) return s;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "tree draft launch");

@@ -8,15 +8,16 @@
 // whose parent it is, in index order) and checks the topology; a node without
 // children has nothing to draft and leaves.  Otherwise the CTA streams the
 // node's draft row once through a ring of shared-memory stages filled by bulk
-// async copies and keeps, per thread,
-//   - the online softmax normaliser (m, sum 2^(z c - fl(m c))), c = log2(e)/T;
-//   - the KM best elements as 64-bit keys (orderable float bits << 32 |
+// async copies and keeps
+//   - per thread, the online softmax normaliser (m, sum 2^(z c - fl(m c))),
+//     c = log2(e)/T;
+//   - per CTA, in shared memory, the n best elements seen so far (n = the
+//     node's number of children) as 64-bit keys (orderable float bits << 32 |
 //     ~index): a larger key is a larger logit, or an equal logit at a smaller
-//     index, so key order is the drafting order.  Elements are offered to the
-//     list only when they reach a bound that no element below it can beat: the
-//     KM-th best key of the warp's lists, or of any warp of the CTA.
-// The lists are merged per warp and then across warps in KM rounds of
-// argmax extraction; child r of the node receives key r.
+//     index, so key order is the drafting order.  An element is offered to
+//     the list only when its value reaches the CTA's bound: the value of the
+//     list's last key, which n distinct elements reach.
+// Child r of the node receives key r of the list.
 #pragma once
 
 #include "common.cuh"
@@ -28,8 +29,7 @@ constexpr int TD_WARPS = TD_THREADS / 32;
 constexpr int TD_MAX_N = 1024;
 constexpr int TD_MAX_CHILDREN = 16;
 constexpr int TD_STAGE = 4 * 16 * TD_THREADS;   // bytes per ring stage: 4 vectors per thread
-constexpr int TD_NS = 4;                    // ring stages
-constexpr int TD_BOUND_EVERY = 4;           // groups between refreshes of the warp's top-KM bound (power of 2)
+constexpr int TD_NS = 3;                    // ring stages (4 CTAs of 256 threads fit an SM)
 
 struct TreeDraftArgs {
   const unsigned char* draft;   // [B, N, V]
@@ -53,89 +53,81 @@ __device__ __forceinline__ unsigned long long td_key(float x, int idx) {
   return (static_cast<unsigned long long>(td_ord(x)) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(idx));
 }
 
-// insert key into the descending list k[0..KM) (the caller checked key > k[KM-1])
-template <int KM>
-__device__ __forceinline__ void td_insert(unsigned long long (&k)[KM], unsigned long long key) {
-  k[KM - 1] = key;
-#pragma unroll
-  for (int j = KM - 1; j > 0; --j) {
-    if (k[j] > k[j - 1]) {
-      const unsigned long long t = k[j];
-      k[j] = k[j - 1];
-      k[j - 1] = t;
-    }
+// element i of a 16-byte vector, without indexing registers at run time
+template <class T>
+__device__ __forceinline__ float td_elem(const uint4& q, int i) {
+  if constexpr (T::esz == 2) {
+    const uint32_t w = (i & 4) ? ((i & 2) ? q.w : q.z) : ((i & 2) ? q.y : q.x);
+    return __uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16));
+  } else {
+    return __uint_as_float((i & 2) ? ((i & 1) ? q.w : q.z) : ((i & 1) ? q.y : q.x));
   }
 }
 
-// KM rounds of warp-wide argmax extraction over the lanes' descending lists;
-// every lane returns the merged top KM in out[] (the lanes' lists are consumed)
-template <int KM>
-__device__ __forceinline__ void td_warp_merge(unsigned long long (&k)[KM], unsigned long long (&out)[KM], int lane) {
-#pragma unroll
-  for (int r = 0; r < KM; ++r) {
-    unsigned long long best = k[0];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    out[r] = best;
-    // keys are unique (they carry the index), except the empty key 0
-    const unsigned win = __ballot_sync(0xffffffffu, k[0] == best);
-    if (lane == __ffs(win) - 1) {
-#pragma unroll
-      for (int j = 0; j + 1 < KM; ++j) k[j] = k[j + 1];
-      k[KM - 1] = 0ull;
-    }
+// Offer a key to the CTA's list top[0..n), kept in descending order.  At each
+// level an atomic maximum leaves the larger of the level's key and the carried
+// one in place, and the smaller is carried to the next level: no key is lost
+// or duplicated, a level only grows, and a key carried into a level never
+// exceeds the level above it, so the list is descending at every moment.  A
+// key carried off the end lost to every key the list then held (and levels
+// only grow), so the list ends as the n best keys offered.  The value of the
+// last key is then published as the CTA's bound: n distinct elements reach it,
+// so an element below it is not among the n best.
+__device__ __forceinline__ void td_offer(unsigned long long* top, unsigned* bound, int n, unsigned long long key) {
+  if (key < *reinterpret_cast<volatile unsigned long long*>(&top[n - 1])) return;   // n listed keys beat it
+#pragma unroll 1
+  for (int j = 0; j < n && key != 0ull; ++j) {
+    const unsigned long long old = atomicMax(&top[j], key);
+    key = old < key ? old : key;
   }
+  const unsigned long long last = *reinterpret_cast<volatile unsigned long long*>(&top[n - 1]);
+  if (last != 0ull) atomicMax(bound, static_cast<unsigned>(last >> 32));
 }
 
-// the KM-th largest key in the union of the warp's lists (0 if the union holds
-// fewer than KM keys): KM rounds of "each lane's largest key below the bound,
-// then the warp's maximum"; keys are unique (they carry the index)
-template <int KM>
-__device__ __forceinline__ unsigned long long td_warp_kth(const unsigned long long (&k)[KM]) {
-  unsigned long long bound = ~0ull, res = 0ull;
+// A first bound for a warp that has seen nothing else: the n-th largest of
+// the lanes' values v, each a distinct element of the row (lanes holding no
+// element pass -inf).  n distinct elements reach it, so nothing below it can
+// be among the n best.  Returns -inf (no bound) when fewer than n lanes hold
+// a finite value.
+__device__ __forceinline__ float td_seed(float v, int n, int lane) {
+  float kth = kNegInf;
+#pragma unroll 1
+  for (int r = 0; r < n; ++r) {
+    float m = v;
 #pragma unroll
-  for (int r = 0; r < KM; ++r) {
-    unsigned long long mine = 0ull;
-#pragma unroll
-    for (int j = KM - 1; j >= 0; --j)
-      if (k[j] < bound) mine = k[j];   // descending list: the last hit is the largest below the bound
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, mine, o);
-      mine = other > mine ? other : mine;
-    }
-    res = mine;
-    bound = mine;
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    kth = m;
+    const unsigned hit = __ballot_sync(0xffffffffu, v == m);
+    if (lane == __ffs(hit) - 1) v = kNegInf;   // one lane per round leaves
   }
-  return res;
+  return kth > kNegInf ? kth : kNegInf;   // a NaN kth (every lane NaN) is no bound either
 }
 
-template <class T, int KM>
-__global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a) {
+template <class T>
+__global__ void __launch_bounds__(TD_THREADS, 4) tree_draft_kernel(TreeDraftArgs a) {
   __shared__ int s_cnt[TD_MAX_N];            // children per node (topology check)
   __shared__ int s_children[TD_MAX_CHILDREN];
   __shared__ int s_wcnt[TD_WARPS];
   __shared__ int s_nchild;
   __shared__ int s_bad;
-  __shared__ unsigned long long s_keys[TD_WARPS][KM];
+  __shared__ unsigned long long s_top[TD_MAX_CHILDREN];   // the CTA's best keys so far, descending
+  __shared__ unsigned s_bound;                            // orderable value they all reach (0: none yet)
   __shared__ float2 s_norm[TD_WARPS];
   extern __shared__ __align__(128) unsigned char s_ring[];   // TD_NS * TD_STAGE bytes (vector rows only)
   __shared__ __align__(8) uint64_t s_full[TD_NS];
   __shared__ __align__(8) uint64_t s_empty[TD_NS];
   __shared__ int s_timeout;
-  __shared__ unsigned long long s_wkey[TD_WARPS];   // each warp's KM-th best key at its last refresh
 
   const int N = a.N, V = a.V;
   const int b = static_cast<int>(blockIdx.x / N), p = static_cast<int>(blockIdx.x % N);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < N; i += TD_THREADS) s_cnt[i] = 0;
+  if (tid < TD_MAX_CHILDREN) s_top[tid] = 0ull;
   if (tid == 0) {
     s_nchild = 0;
     s_bad = 0;
     s_timeout = 0;
+    s_bound = 0u;
   }
   __syncthreads();
   // The topology check runs in every CTA over the whole parent array, so all
@@ -171,7 +163,7 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
   for (int i = tid; i < N; i += TD_THREADS)
     if (s_cnt[i] > a.max_children) s_bad = 1;
   __syncthreads();
-  const int nchild = s_nchild;
+  const int nchild = s_nchild;   // <= max_children <= TD_MAX_CHILDREN unless the topology is bad
   const bool topo_bad = s_bad != 0;
 
   int32_t* tok = a.node_tokens + static_cast<long long>(b) * N;
@@ -196,36 +188,12 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
   const float c = a.c;
   StatsAcc acc;
   acc.init();
-  unsigned long long k[KM];
-#pragma unroll
-  for (int j = 0; j < KM; ++j) k[j] = 0ull;
-  bool full = false;
-  float thr = kNegInf;    // value of the thread's KM-th best once its list is full
-  bool wbound = false;    // some lane of the warp has a full list ...
-  float wthr = kNegInf;   // ... and this is the largest such KM-th value (a bound for every lane)
-
-  // insert the elements of one vector (index e0..) that beat the list
-  auto insert_vec = [&](const float* x, int e0, int cnt) {
-    // one compare per element against the tighter of the two bounds; with
-    // neither (the list is not full and the warp holds fewer than KM keys)
-    // every non-NaN element is examined
-    const bool open = !wbound && !full;
-    const float lim = fmaxf(wbound ? wthr : kNegInf, full ? thr : kNegInf);
-    bool any = false;
-#pragma unroll
-    for (int i = 0; i < T::vpe; ++i) {
-      if (i < cnt && (x[i] >= lim || (open && x[i] == x[i]))) {
-        const unsigned long long key = td_key(x[i], e0 + i);
-        if (key > k[KM - 1]) {
-          td_insert<KM>(k, key);
-          any = true;
-        }
-      }
-    }
-    if (any) {
-      full = k[KM - 1] != 0ull;
-      thr = full ? td_unord(static_cast<uint32_t>(k[KM - 1] >> 32)) : kNegInf;
-    }
+  // the CTA's bound as it stands: it only rises, so a stale read is still a
+  // valid (lower) bound; every bound test admits equal values and the key
+  // comparison orders ties
+  auto bound = [&]() {
+    const unsigned bo = *reinterpret_cast<volatile unsigned*>(&s_bound);
+    return bo != 0u ? td_unord(bo) : kNegInf;
   };
 
   if (a.vec) {
@@ -234,7 +202,7 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
     // full mbarrier per stage counts the bytes, an empty one the warps that
     // are done with it).  A stage is one group of 4 vectors
     // per thread: one packed maximum serves the normaliser (one rescale at most
-    // per group) and the top-k filter; exponents and sums run on packed fp32
+    // per group) and the bound test; exponents and sums run on packed fp32
     // pairs.  Vectors past the row's end read as -inf.
     constexpr int G = 4;
     const int nv = V / T::vpe;
@@ -248,7 +216,6 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
       }
       mbar_fence_init();
     }
-    if (tid < TD_WARPS) s_wkey[tid] = 0ull;
     __syncthreads();
     auto issue = [&](int ch) {   // thread 0
       const int st = ch % TD_NS;
@@ -277,23 +244,6 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
         s_timeout = 1;
         break;
       }
-      if (ch > 0 && ((ch - 1) & (TD_BOUND_EVERY - 1)) == 0) {
-        // every warp's published bound is a bound for the whole CTA (each
-        // warp's KM best are in the CTA's union): take the largest.  Warps
-        // are not in step, so a bound may come from later indices: every
-        // bound test admits equal values and the key comparison orders ties.
-        unsigned long long ck = 0ull;
-#pragma unroll
-        for (int w = 0; w < TD_WARPS; ++w) {
-          const unsigned long long wv = *reinterpret_cast<volatile unsigned long long*>(&s_wkey[w]);
-          ck = wv > ck ? wv : ck;
-        }
-        if (ck != 0ull) {
-          const float cv = td_unord(static_cast<uint32_t>(ck >> 32));
-          wthr = wbound ? fmaxf(wthr, cv) : cv;
-          wbound = true;
-        }
-      }
       const int v0 = ch * (TD_STAGE / 16) + tid;
       uint4 q[G];
       const uint4* sv4 = reinterpret_cast<const uint4*>(s_ring + st * TD_STAGE);
@@ -304,8 +254,7 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
       }
       __syncwarp();   // the warp has its copy of the stage: release it
       if (lane == 0) mbar_arrive(&s_empty[st]);
-      // per-vector maxima (packed for bf16), then the group maximum
-      float vmu[G];
+      // the group maximum (packed for bf16)
       float vm;
       if constexpr (T::esz == 2) {
         uint32_t m4[G];
@@ -313,9 +262,8 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
         for (int u = 0; u < G; ++u) m4[u] = bf16x2_max(bf16x2_max(q[u].x, q[u].y), bf16x2_max(q[u].z, q[u].w));
         const uint32_t mx = bf16x2_max(bf16x2_max(m4[0], m4[1]), bf16x2_max(m4[2], m4[3]));
         vm = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
-#pragma unroll
-        for (int u = 0; u < G; ++u) vmu[u] = fmaxf(__uint_as_float(m4[u] << 16), __uint_as_float(m4[u] & 0xffff0000u));
       } else {
+        float vmu[G];
 #pragma unroll
         for (int u = 0; u < G; ++u)
           vmu[u] = fmaxf(fmaxf(__uint_as_float(q[u].x), __uint_as_float(q[u].y)),
@@ -352,52 +300,37 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
       float s0, s1;
       f2_unpack(s2, s0, s1);
       acc.s += s0 + s1;
+      float thr = bound();
       if (ch == 0) {
-        // No list holds anything yet: seed the bound with the KM-th largest of
-        // the lanes' group maxima (KM distinct elements reach it, so nothing
-        // below it can be in the top KM).  Indices interleave across lanes in
-        // this group, so equal values must still be examined: the bound is
-        // lowered by one ulp, and the bound tests admit equal values anyway.
-        float v = vm, kth = kNegInf;
-#pragma unroll
-        for (int r = 0; r < KM; ++r) {
-          float m = v;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          kth = m;
-          const unsigned hit = __ballot_sync(0xffffffffu, v == m);
-          if (lane == __ffs(hit) - 1) v = kNegInf;   // one lane per round leaves
+        // nothing listed yet: seed the bound from the lanes' group maxima
+        const float kth = td_seed(vm, nchild, lane);
+        if (kth > kNegInf) {
+          if (lane == 0) atomicMax(&s_bound, td_ord(kth));
+          thr = fmaxf(thr, kth);
         }
-        wbound = kth > kNegInf;
-        wthr = wbound ? nextafterf(kth, kNegInf) : kNegInf;
       }
-      // NaN never passes these filters (bf16x2 max skips it; the sum above
-      // turns NaN).  A warp takes this branch whenever one lane does, so the
-      // per-vector test keeps the cost of the lanes that only follow small.
-      if (!wbound || vm >= wthr) {
+      // NaN never passes the tests (bf16x2 max skips it; a NaN maximum fails
+      // the comparison).  The elements that reach the bound are collected as
+      // bits of a mask and offered one by one.
+      if (vm >= thr) {
+        unsigned pass = 0u;
 #pragma unroll
         for (int u = 0; u < G; ++u) {
-          const int v = v0 + u * TD_THREADS;
-          if (v < nv && (!wbound || vmu[u] >= wthr)) {
+          if (v0 + u * TD_THREADS < nv) {
             float x[T::vpe];
             T::unpack(q[u], x);
-            insert_vec(x, v * T::vpe, T::vpe);
+#pragma unroll
+            for (int i = 0; i < T::vpe; ++i)
+              if (x[i] >= thr) pass |= 1u << (u * T::vpe + i);
           }
         }
-      }
-      // The KM-th best key of the union of the warp's lists bounds what can
-      // still enter the warp's (hence the CTA's) top KM.  The bound tests admit
-      // equal values and the key comparison then orders ties by index, so the
-      // filter never drops a member of the top KM; an older bound is lower,
-      // hence still valid, so it is refreshed only every TD_BOUND_EVERY groups.
-      // Until the warp holds KM keys there is no bound and every group is
-      // examined.
-      if ((ch & (TD_BOUND_EVERY - 1)) == 0 || ch < 2) {
-        // the exact bound: the KM-th best key the warp holds
-        const unsigned long long wk = td_warp_kth<KM>(k);
-        wbound = wk != 0ull;
-        wthr = wbound ? td_unord(static_cast<uint32_t>(wk >> 32)) : kNegInf;
-        if (lane == 0) *reinterpret_cast<volatile unsigned long long*>(&s_wkey[warp]) = wk;
+        while (pass != 0u) {
+          const int bit = __ffs(pass) - 1;
+          pass &= pass - 1u;
+          const int u = bit / T::vpe, i = bit - u * T::vpe;
+          const uint4 qq = u == 0 ? q[0] : u == 1 ? q[1] : u == 2 ? q[2] : q[3];
+          td_offer(s_top, &s_bound, nchild, td_key(td_elem<T>(qq, i), (v0 + u * TD_THREADS) * T::vpe + i));
+        }
       }
     }
     __syncthreads();
@@ -416,26 +349,31 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
       return;
     }
   } else {
-    for (int e = tid; e < V; e += TD_THREADS) {
+    // element loads (rows not 16-byte aligned): rounds of one element per
+    // thread, all lanes of a warp in every round
+    for (int base = 0; base < V; base += TD_THREADS) {
+      const int e = base + tid;
       float x[T::vpe];
-      x[0] = T::load(row, e);
+      x[0] = e < V ? T::load(row, e) : kNegInf;
 #pragma unroll
       for (int i = 1; i < T::vpe; ++i) x[i] = kNegInf;
       acc.template add<1>(x, c);
-      if (!full || x[0] > thr) insert_vec(x, e, 1);
+      float thr = bound();
+      if (base == 0) {
+        const float kth = td_seed(x[0], nchild, lane);
+        if (kth > kNegInf) {
+          if (lane == 0) atomicMax(&s_bound, td_ord(kth));
+          thr = fmaxf(thr, kth);
+        }
+      }
+      if (e < V && x[0] >= thr) td_offer(s_top, &s_bound, nchild, td_key(x[0], e));
     }
   }
 
   // ---- merge ----------------------------------------------------------------
   acc.warp_reduce(c);
-  unsigned long long wk[KM];
-  td_warp_merge<KM>(k, wk, lane);
-  if (lane == 0) {
-    s_norm[warp] = acc.pack();
-#pragma unroll
-    for (int j = 0; j < KM; ++j) s_keys[warp][j] = wk[j];
-  }
-  __syncthreads();
+  if (lane == 0) s_norm[warp] = acc.pack();
+  __syncthreads();   // also: every offer to the list has completed
   if (warp != 0) return;
   StatsAcc tot;
   tot.init();
@@ -443,11 +381,6 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
   else tot.unpack(make_float2(kNegInf, 0.f));
   tot.nA = (tot.m == kNegInf) ? 0.f : -__fmul_rn(tot.m, c);
   tot.warp_reduce(c);
-  unsigned long long lk[KM];
-#pragma unroll
-  for (int j = 0; j < KM; ++j) lk[j] = lane < TD_WARPS ? s_keys[lane][j] : 0ull;
-  unsigned long long fk[KM];
-  td_warp_merge<KM>(lk, fk, lane);
 
   // a row is usable iff its maximum is finite and its sum positive and finite
   // (NaN or +inf anywhere poison the sum; no finite entry leaves m = -inf)
@@ -455,10 +388,7 @@ __global__ void __launch_bounds__(TD_THREADS) tree_draft_kernel(TreeDraftArgs a)
   const float A = __fmul_rn(tot.m, c);
   const float l2s = row_ok ? log2f(tot.s) : 0.f;
   for (int r = lane; r < nchild; r += 32) {
-    unsigned long long key = 0ull;
-#pragma unroll
-    for (int j = 0; j < KM; ++j)
-      if (j == r) key = fk[j];
+    const unsigned long long key = s_top[r];
     const int child = s_children[r];
     if (!row_ok || key == 0ull) {
       tok[child] = -1;
