@@ -865,16 +865,17 @@ class StatsWorkload(Workload):
     name = "stats"
     metric = "draft positions scored/s"
     unit = "positions/s"
-    summary = "row_stats_kernel_b256_v128256_k5_bf16.md"
-    kernel = "row_stats_kernel<bf16, bf16 logits>"
+    summary = "row_stats_stream_kernel_b256_v128256_k5_bf16.md"
+    kernel = "row_stats_stream_kernel<bf16>"
     seq_noun = "sequences' statistics"
-    sources = ("common.cuh", "row_stats.cuh")
+    sources = ("common.cuh", "row_stats.cuh", "row_stats_stream.cuh")
 
     def describe(self):
         return {"workload": "acceptance statistics (sum min(p,q), KL(q||p), TV) per drafted position, B=256 "
                             "V=128256 K=5 bf16 T=0.7, the headline sampling inputs", "B": B, "V": V, "K": K,
                 "temperature": T, "input_bytes": 2 * B * K * V * 2,
-                "l2": "inputs (657 MB read) larger than L2; no flush"}
+                "l2": "inputs (657 MB read once from HBM) larger than L2; no flush; the second pass over each "
+                      "pair's rows is meant to hit L2 (DRAM traffic in profiles/)"}
 
     def batch(self, seqs):
         from speculative_decoding_verification_52_gb300 import inputs as gen

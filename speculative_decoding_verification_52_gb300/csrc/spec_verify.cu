@@ -28,6 +28,7 @@
 #include "tree_mask.cuh"
 #include "kv_commit.cuh"
 #include "row_stats.cuh"
+#include "row_stats_stream.cuh"
 #include "tree_draft.cuh"
 
 namespace {
@@ -736,6 +737,24 @@ spec_status_t launch_row_stats(int dev, const RowStatsArgs& a, cudaStream_t st) 
   return SPEC_OK;
 }
 
+// logits rows of one dtype that bulk copies can stream: one persistent CTA per
+// SM, two passes over each position pair's rows (no exchange between CTAs)
+template <class T>
+spec_status_t launch_row_stats_stream(int dev, int sms, const RowStatsArgs& a, cudaStream_t st) {
+  auto kern = row_stats_stream_kernel<T>;
+  constexpr int smem = RT_NS * RT_STAGE;
+  if (!once_per_device(dev, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
+      }))
+    return fail(SPEC_ERR_CUDA, "row stats kernel setup failed: %s", cudaGetErrorString(cudaGetLastError()));
+  const long long pairs = static_cast<long long>(a.B) * a.K;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(pairs, std::max(1, sms)));
+  kern<<<grid, RT_THREADS, smem, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "row stats launch");
+  return SPEC_OK;
+}
+
 // ---------------------------------------------------------------------------
 // top-k tree drafting
 // ---------------------------------------------------------------------------
@@ -1082,7 +1101,10 @@ spec_status_t spec_row_stats(const void* target_logits, spec_dtype_t target_dtyp
     a.tv = tv;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     prof_mark(0, st);
-    if (probs)
+    if (!probs && a.vec && target_dtype == draft_dtype)
+      s = target_dtype == SPEC_BF16 ? launch_row_stats_stream<BF16T>(dev, di.sms, a, st)
+                                    : launch_row_stats_stream<F32T>(dev, di.sms, a, st);
+    else if (probs)
       s = target_dtype == SPEC_BF16 ? launch_row_stats<BF16T, F32T, true>(dev, a, st)
                                     : launch_row_stats<F32T, F32T, true>(dev, a, st);
     else if (target_dtype == SPEC_BF16)
