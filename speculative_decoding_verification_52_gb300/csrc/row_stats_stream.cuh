@@ -65,15 +65,23 @@ __device__ __forceinline__ float rt_raise(float vm, float c, float& m, float& nA
   return f;
 }
 
-// the maximum of one vector of elements (fp32; NaN is skipped: it reaches the
-// sums instead)
+// the maximum of a thread's vectors of one row (fp32; NaN is skipped: it
+// reaches the sums instead); bf16 words are reduced packed, then unpacked once
 template <class T>
-__device__ __forceinline__ float rt_vmax(const uint4& q) {
+__device__ __forceinline__ float rt_vmax(const uint4 (&q)[RT_VPT]) {
   if constexpr (T::esz == 2) {
-    const uint32_t mx = bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w));
+    uint32_t mx = bf16x2_max(bf16x2_max(q[0].x, q[0].y), bf16x2_max(q[0].z, q[0].w));
+#pragma unroll
+    for (int u = 1; u < RT_VPT; ++u)
+      mx = bf16x2_max(mx, bf16x2_max(bf16x2_max(q[u].x, q[u].y), bf16x2_max(q[u].z, q[u].w)));
     return fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
   } else {
-    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)), fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+    float m = kNegInf;
+#pragma unroll
+    for (int u = 0; u < RT_VPT; ++u)
+      m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(q[u].x), __uint_as_float(q[u].y)),
+                         fmaxf(__uint_as_float(q[u].z), __uint_as_float(q[u].w))));
+    return m;
   }
 }
 
@@ -162,11 +170,20 @@ __global__ void __launch_bounds__(RT_THREADS, 1) row_stats_stream_kernel(RowStat
     const int nv = static_cast<int>(min(static_cast<long long>(E), V - static_cast<long long>(ch) * E)) / T::vpe;
     const uint4* tb = reinterpret_cast<const uint4*>(rt_ring + stage * RT_STAGE);
     const uint4* db = reinterpret_cast<const uint4*>(rt_ring + stage * RT_STAGE + RT_STAGE / 2);
+    // (after a timeout the stage's bytes are garbage; the pair is marked anyway)
+    if (nv == E / T::vpe) {   // a full chunk (all but a row's last): no bounds to test
 #pragma unroll
-    for (int u = 0; u < RT_VPT; ++u) {
-      const int v = ctid + u * RT_CT;
-      zt[u] = (!tmo && v < nv) ? tb[v] : ninf4;
-      yt[u] = (!tmo && v < nv) ? db[v] : ninf4;
+      for (int u = 0; u < RT_VPT; ++u) {
+        zt[u] = tb[ctid + u * RT_CT];
+        yt[u] = db[ctid + u * RT_CT];
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < RT_VPT; ++u) {
+        const int v = ctid + u * RT_CT;
+        zt[u] = v < nv ? tb[v] : ninf4;
+        yt[u] = v < nv ? db[v] : ninf4;
+      }
     }
     __syncwarp();
     if (lane == 0 && !tmo) mbar_arrive(&sh.empty[stage]);
@@ -180,12 +197,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) row_stats_stream_kernel(RowStat
     for (int ch = 0; ch < nch; ++ch) {
       uint4 zt[RT_VPT], yt[RT_VPT];
       take(ch, zt, yt);
-      float vp = rt_vmax<T>(zt[0]), vq = rt_vmax<T>(yt[0]);
-#pragma unroll
-      for (int u = 1; u < RT_VPT; ++u) {
-        vp = fmaxf(vp, rt_vmax<T>(zt[u]));
-        vq = fmaxf(vq, rt_vmax<T>(yt[u]));
-      }
+      const float vp = rt_vmax<T>(zt), vq = rt_vmax<T>(yt);
       const float fp = rt_raise(vp, c, mp, np);
       const float fq = rt_raise(vq, c, mq, nq);
       if (fp != 1.f) sp2 = f2_fma(sp2, f2_pack(fp, fp), f2_pack(0.f, 0.f));
