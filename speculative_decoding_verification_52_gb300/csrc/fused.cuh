@@ -61,6 +61,7 @@ constexpr int FU_MERGE_WARP = FU_CW + 1;
 constexpr int FU_FIN_WARP = FU_CW + 2;
 constexpr int FU_STAGE = 16384;
 constexpr int FU_VPT = (FU_STAGE / 16 + FU_CT - 1) / FU_CT;   // 16-byte vectors per consumer thread per stage
+static_assert((FU_VPT - 1) * FU_CT <= FU_STAGE / 16, "a full stage covers every consumer thread's first FU_VPT-1 vectors");
 constexpr int FU_NSTAGE = 4;
 constexpr int FU_CTAS_PER_SM = 3;
 constexpr int FU_MAX_GRID = 1024;                 // persistent grid cap
@@ -289,10 +290,19 @@ __device__ __forceinline__ float exp2_arg_ff(float z, float c, float A) {
 // packed fp32 pairs
 __device__ __forceinline__ void stats_stage_bf16(const uint4* buf, int nvec, int ctid, float c, StatsAcc& acc) {
   uint4 q[FU_VPT];
+  if (nvec == FU_STAGE / 16) {   // a full stage: only the last vector may lie past its end
 #pragma unroll
-  for (int k = 0; k < FU_VPT; ++k) {
-    const int v = ctid + k * FU_CT;
-    q[k] = v < nvec ? buf[v] : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+    for (int k = 0; k < FU_VPT; ++k) {
+      const int v = ctid + k * FU_CT;
+      q[k] = (k + 1 < FU_VPT || v < FU_STAGE / 16) ? buf[v]
+                                                    : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < FU_VPT; ++k) {
+      const int v = ctid + k * FU_CT;
+      q[k] = v < nvec ? buf[v] : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+    }
   }
   uint32_t mx = bf16x2_max(bf16x2_max(q[0].x, q[0].y), bf16x2_max(q[0].z, q[0].w));
 #pragma unroll
