@@ -765,7 +765,7 @@ class TreeMaskWorkload(Workload):
     metric = "tree-attention mask rows/s"
     unit = "rows/s"
     summary = "tree_mask_kernel_b4096_n256.md"
-    kernel = "tree_mask_reg_kernel<8>"
+    kernel = "tree_mask_run_kernel<8>"
     seq_noun = "trees masked"
     sources = ("tree_mask.cuh",)
     dtype = oracle_dtype = "u32"

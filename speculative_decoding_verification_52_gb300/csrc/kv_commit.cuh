@@ -53,9 +53,19 @@ __global__ void __launch_bounds__(KV_THREADS) kv_commit_kernel(const KvCommitArg
     const unsigned char* src = a.scratch + (static_cast<unsigned long long>(b) * a.N + s) * a.E;
     unsigned char* dst = a.cache + (static_cast<unsigned long long>(b) * a.Lmax + L + j) * a.E;
     if (a.vec) {
+      // four loads in flight per thread before their stores
       const uint4* s4 = reinterpret_cast<const uint4*>(src);
       uint4* d4 = reinterpret_cast<uint4*>(dst);
-      for (unsigned long long k = threadIdx.x; k < a.E / 16; k += KV_THREADS) d4[k] = __ldcs(s4 + k);
+      const unsigned long long nv = a.E / 16;
+      unsigned long long k = threadIdx.x;
+      for (; k + 3 * KV_THREADS < nv; k += 4 * KV_THREADS) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldcs(s4 + k + u * KV_THREADS);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) d4[k + u * KV_THREADS] = v[u];
+      }
+      for (; k < nv; k += KV_THREADS) d4[k] = __ldcs(s4 + k);
     } else {
       for (unsigned long long k = threadIdx.x; k < a.E; k += KV_THREADS) dst[k] = src[k];
     }

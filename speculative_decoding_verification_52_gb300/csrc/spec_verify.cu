@@ -995,16 +995,17 @@ spec_status_t spec_tree_mask(const int32_t* parents, int B, int N, uint32_t* mas
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int NW = (N + 31) / 32;
     const int grid = std::min(B, di.sms * 16);
-    const size_t psmem = sizeof(int) * static_cast<size_t>(N);
-    // rows in registers for up to 16 words (the output base must allow the
+    const size_t psmem = (sizeof(int) * static_cast<size_t>(N) + 15) & ~size_t(15);
+    // rows of up to 16 words built run by run (the output base must allow the
     // vector stores: rows of NW words are then 4 * NW-byte aligned)
     const bool vec = (reinterpret_cast<uintptr_t>(masks) & 15u) == 0;
+    auto rsmem = [&](int nwt) { return psmem + sizeof(uint32_t) * TM_THREADS * static_cast<size_t>(nwt); };
     prof_mark(0, st);
-    if (vec && NW == 1) tree_mask_reg_kernel<1><<<grid, TM_THREADS, psmem, st>>>(parents, B, N, masks, status);
-    else if (vec && NW == 2) tree_mask_reg_kernel<2><<<grid, TM_THREADS, psmem, st>>>(parents, B, N, masks, status);
-    else if (vec && NW <= 4) tree_mask_reg_kernel<4><<<grid, TM_THREADS, psmem, st>>>(parents, B, N, masks, status);
-    else if (vec && NW <= 8) tree_mask_reg_kernel<8><<<grid, TM_THREADS, psmem, st>>>(parents, B, N, masks, status);
-    else if (vec && NW <= 16) tree_mask_reg_kernel<16><<<grid, TM_THREADS, psmem, st>>>(parents, B, N, masks, status);
+    if (vec && NW == 1) tree_mask_run_kernel<1><<<grid, TM_THREADS, rsmem(1), st>>>(parents, B, N, masks, status);
+    else if (vec && NW == 2) tree_mask_run_kernel<2><<<grid, TM_THREADS, rsmem(2), st>>>(parents, B, N, masks, status);
+    else if (vec && NW <= 4) tree_mask_run_kernel<4><<<grid, TM_THREADS, rsmem(4), st>>>(parents, B, N, masks, status);
+    else if (vec && NW <= 8) tree_mask_run_kernel<8><<<grid, TM_THREADS, rsmem(8), st>>>(parents, B, N, masks, status);
+    else if (vec && NW <= 16) tree_mask_run_kernel<16><<<grid, TM_THREADS, rsmem(16), st>>>(parents, B, N, masks, status);
     else {
       const size_t smem = psmem + sizeof(uint32_t) * TM_THREADS * NW;
       tree_mask_kernel<<<std::min(B, di.sms * 8), TM_THREADS, smem, st>>>(parents, B, N, masks, status);

@@ -8,7 +8,9 @@
 // 0 <= parents[i] < i); then each thread builds the masks of its rows, one at a
 // time, in a private shared-memory row of NW = ceil(N/32) words by walking from
 // the node up to the root, and writes the row out (the rows of consecutive
-// threads are consecutive in memory, so the stores coalesce).
+// threads are consecutive in memory, so the stores coalesce).  Rows of up to 16
+// words take tree_mask_run_kernel (one store per word run of the walk, vector
+// stores out); longer rows the general tree_mask_kernel.
 #pragma once
 
 #include "common.cuh"
@@ -48,16 +50,20 @@ __global__ void __launch_bounds__(TM_THREADS) tree_mask_kernel(const int32_t* __
   }
 }
 
-// The same walk with the row held in registers (up to NWT words, a
-// compile-time count, so every word access is a register select) and written
-// with vector stores when the row is exactly NWT words: one thread per row, the
-// sequence's parents in shared memory.
+// The walk visits its nodes in decreasing order (parents[i] < i), so the words
+// of the row are visited in non-increasing order and each word's bits form one
+// run of the walk: the run's bits gather in one register and are stored once,
+// into the thread's row in shared memory (zeroed first), when the walk moves to
+// a lower word.  A step costs a shift, an OR and a compare instead of a select
+// over every word of the row; the row then goes out with vector stores.
 template <int NWT>
-__global__ void __launch_bounds__(TM_THREADS) tree_mask_reg_kernel(const int32_t* __restrict__ parents, int B, int N,
+__global__ void __launch_bounds__(TM_THREADS) tree_mask_run_kernel(const int32_t* __restrict__ parents, int B, int N,
                                                                    uint32_t* __restrict__ out,
                                                                    int32_t* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char tm_smem[];
   int* par = reinterpret_cast<int*>(tm_smem);
+  uint32_t* row = reinterpret_cast<uint32_t*>(tm_smem + ((static_cast<size_t>(N) * sizeof(int) + 15) & ~size_t(15))) +
+                  threadIdx.x * NWT;
   for (int b = blockIdx.x; b < B; b += gridDim.x) {
     const int32_t* pb = parents + static_cast<long long>(b) * N;
     bool ok = true;
@@ -70,24 +76,32 @@ __global__ void __launch_bounds__(TM_THREADS) tree_mask_reg_kernel(const int32_t
     const int NW = (N + 31) / 32;   // the row stride; NW <= NWT
     uint32_t* ob = out + static_cast<long long>(b) * N * NW;
     for (int i = threadIdx.x; i < N; i += TM_THREADS) {
-      uint32_t row[NWT];
+      if constexpr (NWT % 4 == 0) {
 #pragma unroll
-      for (int w = 0; w < NWT; ++w) row[w] = 0u;
+        for (int w = 0; w < NWT; w += 4) reinterpret_cast<uint4*>(row)[w / 4] = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+#pragma unroll
+        for (int w = 0; w < NWT; ++w) row[w] = 0u;
+      }
       if (ok) {
+        int cw = i >> 5;
+        uint32_t run = 0u;
         for (int node = i; node >= 0; node = par[node]) {
           const int wn = node >> 5;
-          const uint32_t bit = 1u << (node & 31);
-#pragma unroll
-          for (int w = 0; w < NWT; ++w) row[w] |= (w == wn) ? bit : 0u;
+          if (wn != cw) {
+            row[cw] = run;
+            cw = wn;
+            run = 0u;
+          }
+          run |= 1u << (node & 31);
         }
+        row[cw] = run;
       }
       uint32_t* orow = ob + static_cast<long long>(i) * NW;
       if (NW == NWT && NWT % 4 == 0) {
 #pragma unroll
         for (int w = 0; w < NWT; w += 4)
-          reinterpret_cast<uint4*>(orow)[w / 4] = make_uint4(row[w], row[w + 1], row[w + 2], row[w + 3]);
-      } else if (NW == NWT && NWT == 2) {
-        reinterpret_cast<uint2*>(orow)[0] = make_uint2(row[0], row[NWT - 1]);
+          reinterpret_cast<uint4*>(orow)[w / 4] = reinterpret_cast<const uint4*>(row)[w / 4];
       } else {
 #pragma unroll
         for (int w = 0; w < NWT; ++w)

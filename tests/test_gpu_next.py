@@ -43,7 +43,7 @@ def test_tree_mask_random_per_sequence_trees(orc, N):
     assert rst[9] == -1
 
 
-@pytest.mark.parametrize("E,vec", [(64, True), (4096, True), (6, False), (1000, False)])
+@pytest.mark.parametrize("E,vec", [(64, True), (4096, True), (20000, True), (6, False), (1000, False)])
 def test_kv_commit_matches_oracle(orc, E, vec):
     rng = np.random.default_rng(E)
     B, Lmax, N, W = 24, 40, 9, 6
