@@ -54,7 +54,7 @@
 
 namespace sv {
 
-constexpr int FU_CW = 7;                          // consumer warps
+constexpr int FU_CW = 8;                          // consumer warps (4 vectors each per stage)
 constexpr int FU_CT = FU_CW * 32;
 constexpr int FU_THREADS = FU_CT + 96;            // + producer, merger and finisher warps
 constexpr int FU_MERGE_WARP = FU_CW + 1;
