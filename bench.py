@@ -480,8 +480,8 @@ class AcceptanceWorkload(Workload):
     name = "acceptance"
     metric = "draft positions scored and verified/s"
     unit = "positions/s"
-    kernel = "row_stats_stream_kernel + fused_sample_kernel (f32, V=2048)"
-    sources = ("common.cuh", "row_stats.cuh", "row_stats_stream.cuh", "fused.cuh")
+    kernel = "row_stats_kernel (a cluster of one per pair) + fused_sample_kernel (f32, V=2048)"
+    sources = ("common.cuh", "row_stats.cuh", "fused.cuh")
     SIGMAS = (0.1, 0.3, 0.6, 1.0, 2.0)
     NSEQ, VV = 10_000, 2048
     COPY = (0.04, 0.42, 0.81)      # draft row = target row w.p. c (alpha ~ 0.5, 0.7, 0.9 at T=1)

@@ -264,9 +264,10 @@ spec_status_t spec_kv_commit(void *cache, const int32_t *lengths, const void *sc
  *   three means an internal wait hit its time limit.
  *
  * Each row pair is read from HBM once.  Draft logits of the target's dtype in
- * rows that 16-byte bulk copies can stream go through one CTA per SM that
- * reads each pair twice, the second time from L2; every other case through one
- * thread-block cluster per pair that holds it in shared memory.  Limits:
+ * rows that 16-byte bulk copies can stream and that exceed 64 KB per pair go
+ * through one CTA per SM that reads each pair twice, the second time from L2;
+ * every other case through one thread-block cluster per pair that holds it in
+ * shared memory.  Limits:
  * V * (target + draft element bytes) <= 1.6 MB, i.e. V <= 409600 for bf16
  * pairs (SPEC_ERR_UNSUPPORTED beyond); 1e-4 <= T. */
 spec_status_t spec_row_stats(const void *target_logits, spec_dtype_t target_dtype, const void *draft,

@@ -1102,7 +1102,11 @@ spec_status_t spec_row_stats(const void* target_logits, spec_dtype_t target_dtyp
     a.tv = tv;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     prof_mark(0, st);
-    if (!probs && a.vec && target_dtype == draft_dtype)
+    // The streaming kernel takes logits rows of one dtype that bulk copies can
+    // stream and that do not fit one CTA's slice; a pair that fits one CTA is
+    // cheaper in the cluster kernel (a cluster of one: no exchange, and every
+    // pair a CTA of its own).
+    if (!probs && a.vec && target_dtype == draft_dtype && a.CS > 1)
       s = target_dtype == SPEC_BF16 ? launch_row_stats_stream<BF16T>(dev, di.sms, a, st)
                                     : launch_row_stats_stream<F32T>(dev, di.sms, a, st);
     else if (probs)

@@ -123,9 +123,9 @@ def _stats_pair(orc, target, tdt, draft, ddt, T, probs=False):
                                      (37, "f32"), (77777, "bf16"), (8, "f32"), (40000, "f32"),
                                      (65544, "bf16")])
 def test_row_stats_match_oracle(orc, V, dtype):
-    """The streaming kernel (aligned rows; 65544 bf16 ends in an 8-element
-    chunk) and the cluster kernel (odd V: element loads; cluster sizes 8, 4
-    and 1)."""
+    """The streaming kernel (aligned rows of more than 64 KB per pair; 65544
+    bf16 ends in an 8-element chunk) and the cluster kernel (shorter rows: a
+    cluster of one; odd V: element loads, clusters of 8, 4 and 1)."""
     b = gen.gaussian_chain(6, V, 5, sigma=0.445, T=0.7, dtype=dtype, seed=52_310 + V)
     _stats_pair(orc, b.target, dtype, b.draft, dtype, 0.7)
 
@@ -164,8 +164,8 @@ def test_row_stats_identical_and_controlled(orc):
 
 @pytest.mark.parametrize("V", [4096, 40000])
 def test_row_stats_invalid_rows(orc, V):
-    """Both sizes through the streaming kernel; at V=40000 the NaN sits in the
-    row's last chunk."""
+    """V=4096 through the cluster kernel (one CTA per pair), V=40000 through
+    the streaming kernel, with the NaN in the row's last chunk."""
     b = gen.gaussian_chain(4, V, 3, sigma=0.5, T=1.0, dtype="f32", seed=52_390)
     t, d = b.target.copy(), b.draft.copy()
     t[0, 1, V - 100] = np.nan
