@@ -13,18 +13,24 @@
 //                 (p alone for the bonus row) of one slice of the stopping row
 //                 pair, summed per block of 256 elements.  A producer takes its
 //                 next residual unit as soon as sequence b is ready (its accept
-//                 scan is done), ahead of its next sweep unit, so the stopping
-//                 rows are re-read while still in L2.
+//                 scan is done), ahead of its next sweep unit, so a finished
+//                 sequence's draw does not wait behind the rest of the sweep.
 // Roles inside a CTA:
 //   producer   (1 thread) streams work-item bytes into a ring of FU_NSTAGE 16 KB
 //              shared-memory stages with 1-D bulk async copies (cp.async.bulk,
 //              completion counted on an mbarrier per stage) and writes a small
 //              descriptor per stage.
-//   consumers  (8 warps) each reduce their share of every stage.  At the end of
-//              a work item every warp writes its own partial; the warps count
-//              themselves in shared memory and the last one adds the item to
-//              the sequence's global counter with a fire-and-forget release
-//              reduction.
+//   consumers  (FU_CW warps) each reduce their share of every stage.  At the
+//              end of a work item every warp leaves its partial in shared
+//              memory and the warps count themselves there; the last one hands
+//              a sweep unit to the merger warp, or adds a residual unit to the
+//              sequence's counter with a fire-and-forget release reduction.
+//   merger     (1 warp) clears this CTA's share of the control block before the
+//              grid barrier; then merges the warp partials of completed sweep
+//              units, stores each unit's partial and adds it to the sequence's
+//              counter (release), off the consumers' path, and polls the
+//              readiness word of the sequence the producer wants residual units
+//              of.
 //   finisher   (1 warp) owns a fixed set of sequences: the accept scan of b runs
 //              on CTA b mod grid, the pick of b on CTA (b + grid/2) mod grid.
 //              It polls those sequences' counters; the scan merges the partials
