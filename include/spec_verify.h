@@ -284,8 +284,8 @@ spec_status_t spec_row_stats(const void *target_logits, spec_dtype_t target_dtyp
  *       the draft's distribution for the token after node p (rows of leaves are
  *       not read).
  *   parents [N] int32 (device): parents[0] = -1, 0 <= parents[i] < i.
- *   max_children: 1..16, the most children any node has (it sizes the
- *       per-thread candidate lists).
+ *   max_children: 1..16, the most children any node may have (a node with
+ *       more makes the topology invalid, below).
  *   temperature: > 0; only the log-probabilities depend on it.
  *   node_tokens [B, N] int32 (device, written): the children of node p, in
  *       increasing node index, take the tokens of row p in decreasing logit
