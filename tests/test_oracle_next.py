@@ -218,6 +218,20 @@ def test_tree_draft_matches_numpy_topk(orc, dtype):
             np.testing.assert_allclose(lq[b, kids], log_softmax(zz[b, p] / T)[want], atol=1e-12)
 
 
+def test_tree_draft_flat_rows_take_the_smallest_indices(orc):
+    """A row of equal logits: every token ties, so the children take tokens
+    0, 1, 2, ... in node order, each with log q = -ln V (uniform)."""
+    par = gen.bfs_tree([5, 3], None)
+    B, N, V = 2, len(par), 300
+    z = np.full((B, N, V), 1.25, np.float32)
+    tok, lq, _ = orc.tree_draft(z, "f32", par, 0.9)
+    for p in range(N):
+        kids = [i for i in range(N) if par[i] == p]
+        if kids:
+            assert tok[:, kids].tolist() == [list(range(len(kids)))] * B
+            np.testing.assert_allclose(lq[:, kids], -np.log(V), atol=1e-12)
+
+
 def test_tree_draft_chain_is_greedy_and_perfect_draft_is_accepted(orc):
     """A chain tree drafts the argmax at every step; with the target equal to
     the draft, greedy tree verification accepts the whole tree depth along the
